@@ -1,0 +1,172 @@
+/*
+ * moe_layout.h -- C ABI of the single-GPU MoE layout / dispatch / combine
+ * library (libmoe_layout.so, CUDA, sm_103a).
+ *
+ * The operations follow Perplexity, "Enabling trillion-parameter models on
+ * AWS EFA" (2025-11-04).  The page splits MoE routing into a dispatch that
+ * takes the tokens and their per-token experts and packs each token into
+ * contiguous per-destination buffers, and its dual, combine, that brings the
+ * processed rows back and forms their routing-weighted average (sections
+ * "MoE all-to-all over EFA" and "Dispatch and Combine").  Here the R
+ * expert-parallel destinations are R row ranges of one packed buffer in the
+ * GPU's own memory; there is no network, peer or collective.
+ *
+ * Conventions for every call:
+ *  - All pointers are device pointers unless stated otherwise.  The caller
+ *    allocates and owns every buffer; the library allocates nothing, keeps no
+ *    state between calls and never synchronises.
+ *  - Every call is asynchronous on `stream` (0 = legacy default stream) and
+ *    may be captured into a CUDA graph.
+ *  - Arguments are checked on the host before anything is enqueued.  A
+ *    failed check returns an error status and enqueues nothing.
+ *  - Matrices are row-major and dense: a [rows, H] matrix has row stride H.
+ *  - bf16 means IEEE binary32 truncated to its top 16 bits (stored as 2-byte
+ *    words); e4m3 means the 8-bit "fn" float format (bias 7, largest finite
+ *    448, no infinities).
+ *  - Indices are int32: T*K must stay below 2^31.
+ *  - Notation: T tokens, H hidden size, E experts, R destination ranks,
+ *    K experts per token, Epr = E/R experts per rank.  Expert e belongs to
+ *    rank e / Epr.
+ */
+#ifndef MOE_LAYOUT_H
+#define MOE_LAYOUT_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status returned synchronously by every call. */
+typedef enum moe_status {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,  /* null pointer, size out of range, E % R != 0 ... */
+    MOE_ERR_ALIGNMENT = 2,    /* a pointer misses its required alignment       */
+    MOE_ERR_CUDA = 3,         /* the CUDA runtime refused a launch             */
+    MOE_ERR_WORKSPACE = 4     /* workspace missing or smaller than required    */
+} moe_status_t;
+
+/* Bits of the device error word written by moe_layout (read it after the
+ * stream has reached that point). */
+#define MOE_DEV_ERR_EXPERT_RANGE 1u  /* some topk_ids entry is outside [0, E)   */
+#define MOE_DEV_ERR_DUPLICATE    2u  /* some token lists one expert twice       */
+
+/* Limits of this implementation. */
+#define MOE_MAX_EXPERTS 1024
+#define MOE_MAX_TOPK 32
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char *moe_status_string(moe_status_t status);
+
+/* Bytes of device workspace moe_layout needs for these sizes (0 when the
+ * whole layout fits one thread block).  Returns 0 for invalid sizes, which
+ * moe_layout then rejects. */
+size_t moe_layout_workspace_bytes(int32_t T, int32_t K, int32_t E);
+
+/*
+ * moe_layout -- routing histogram, exclusive scan and stable slot map.
+ *
+ * The page's dispatch-send first counts tokens per expert in shared memory,
+ * then takes the cumulative sum of the counts to find the offsets at which
+ * tokens are packed into contiguous per-destination send buffers ("Dispatch
+ * and Combine"); the per-expert counts are also the routing information that
+ * ranks exchange before writing ("Send/receive buffers").  This call computes
+ * that metadata for all T*K (token, k) entries:
+ *
+ *   expert_counts[e]  = #{(t,k) : topk_ids[t,k] == e}                      [E]
+ *   expert_offsets[e] = sum of expert_counts[e'] for e' < e;
+ *   expert_offsets[E] = number of valid entries (T*K when no error)       [E+1]
+ *   rank_offsets[r]   = expert_offsets[r*Epr]                              [R+1]
+ *   dst_row[t,k]      = expert_offsets[e] + #{(t',k') before (t,k) in
+ *                       row-major order with topk_ids[t',k'] == e}         [T*K]
+ *   src_token[row]    = t for row = dst_row[t,k]                           [T*K]
+ *
+ * So packed row ranges [expert_offsets[e], expert_offsets[e+1]) hold expert
+ * e's tokens in ascending token order, and rank r's region is rows
+ * [rank_offsets[r], rank_offsets[r+1]).
+ *
+ * topk_ids     [T,K] int32, 4-byte aligned.
+ * T >= 0, 1 <= K <= min(E, MOE_MAX_TOPK), 1 <= E <= MOE_MAX_EXPERTS,
+ * R >= 1 with E % R == 0, T*K < 2^31.
+ * Outputs (int32, 4-byte aligned): expert_counts, expert_offsets,
+ * rank_offsets, src_token, dst_row.  dst_row and src_token may be NULL only
+ * when T == 0.
+ * dev_error    [1] uint32 or NULL.  Overwritten with MOE_DEV_ERR_* bits.
+ *              An id outside [0,E) is not counted, gets dst_row -1 and no
+ *              src_token row; src_token rows at or after expert_offsets[E]
+ *              are then left untouched.  A duplicated id still gets its own
+ *              slot, in k order.
+ * workspace    device scratch of at least moe_layout_workspace_bytes(T,K,E)
+ *              bytes, 16-byte aligned (may be NULL when that is 0).  Its
+ *              contents on entry do not matter; it is in use until the
+ *              stream passes this call.
+ * T == 0 writes zero counts and offsets.
+ */
+moe_status_t moe_layout(const int32_t *topk_ids, int32_t T, int32_t K,
+                        int32_t E, int32_t R,
+                        int32_t *expert_counts, int32_t *expert_offsets,
+                        int32_t *rank_offsets, int32_t *src_token,
+                        int32_t *dst_row, uint32_t *dev_error,
+                        void *workspace, size_t workspace_bytes,
+                        cudaStream_t stream);
+
+/*
+ * moe_dispatch -- pack every token row into each of its K slots.
+ *
+ * The page's dispatch sender shuffles the tokens into send buffers so that
+ * each destination receives one contiguous write ("Dispatch and Combine"),
+ * and the evaluated setting quantises that payload to block-scaled FP8
+ * ("Evaluation").  For every token t and k with 0 <= dst_row[t,k] < T*K:
+ *
+ *   fp8 == 0:  packed[dst_row[t,k], :] = tokens[t, :]            (bit copy)
+ *   fp8 == 1:  for each 1x128 block b of row t:
+ *                amax  = max |tokens[t, 128b .. 128b+127]|       (fp32)
+ *                scale = amax / 448                              (fp32, RN)
+ *                packed[dst_row[t,k], 128b+j] =
+ *                    e4m3_satfinite_rn(tokens[t,128b+j] / scale) (fp32 divide)
+ *                scales[dst_row[t,k], b] = scale
+ *              a block with amax == 0 stores scale 0 and codes 0x00 / 0x80
+ *              (the sign of each zero).
+ * Entries with dst_row outside [0, T*K) are skipped.
+ *
+ * tokens   [T,H] bf16, 16-byte aligned.   dst_row [T,K] int32 (moe_layout).
+ * packed   [T*K,H] bf16 (fp8 == 0) or e4m3 bytes (fp8 == 1), 16-byte aligned.
+ * scales   [T*K,H/128] fp32, 4-byte aligned; required when fp8 == 1,
+ *          ignored otherwise.
+ * H >= 8 with H % 8 == 0 (H % 128 == 0 when fp8 == 1).  T == 0 is a no-op.
+ */
+moe_status_t moe_dispatch(const void *tokens, int32_t T, int32_t H, int32_t K,
+                          const int32_t *dst_row, int32_t fp8, void *packed,
+                          float *scales, cudaStream_t stream);
+
+/*
+ * moe_combine -- routing-weighted sum of each token's K expert outputs.
+ *
+ * The page's combine receives the processed rows of every token and computes
+ * their weighted average, accumulating only on the receiving side ("MoE
+ * all-to-all over EFA", "Dispatch and Combine", "Evaluation").  With router
+ * weights that already sum to one the weighted sum is that average, so no
+ * division by the weight sum is made:
+ *
+ *   acc = +0 (fp32);  for k = 0 .. K-1:  acc = fma(topk_weights[t,k],
+ *                                              expert_out[dst_row[t,k], j], acc)
+ *   out[t, j] = bf16 round-to-nearest-even(acc)
+ *
+ * Terms whose dst_row is outside [0, T*K) are skipped.
+ *
+ * expert_out    [T*K,H] bf16, 16-byte aligned (rows in dispatch order).
+ * topk_weights  [T,K] fp32, 4-byte aligned.   dst_row [T,K] int32.
+ * out           [T,H] bf16, 16-byte aligned; must not overlap expert_out.
+ * H >= 8 with H % 8 == 0.  T == 0 is a no-op.
+ */
+moe_status_t moe_combine(const void *expert_out, const float *topk_weights,
+                         const int32_t *dst_row, int32_t T, int32_t H,
+                         int32_t K, void *out, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_LAYOUT_H */

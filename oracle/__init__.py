@@ -1,0 +1,196 @@
+"""CPU oracle for MoE layout, dispatch and combine (ctypes wrapper).
+
+TEST INFRASTRUCTURE ONLY.  This package is the parity reference for the CUDA
+library.  Only ``tests/``, ``__graft_entry__.smoke()`` and the benchmark's
+CPU-baseline / reference leg may import it.  The library package never does,
+and it shares no code with the CUDA sources.
+
+The arithmetic lives in ``moe_oracle.c`` (plain single-threaded C, built with
+``-ffp-contract=off``); this module only compiles it, loads it and marshals
+numpy arrays.  Method source: Perplexity, "Enabling trillion-parameter models
+on AWS EFA", sections "Send/receive buffers", "Dispatch and Combine" and
+"Evaluation".
+
+Parity pins (all CPU tests): the bf16 and e4m3 codecs against PyTorch's own
+conversions (exhaustive decode, constructed ties for encode); the layout
+against numpy's stable argsort and brute force over all tiny routings; bf16
+dispatch by bit identity; FP8 dispatch by the closed-form error bound of the
+block scale; combine against exact rational arithmetic of the fused
+multiply-add chain and against the identity round trip.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "moe_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+CFLAGS = ["-O2", "-ffp-contract=off", "-fno-fast-math", "-std=c11", "-Wall",
+          "-shared", "-fPIC"]
+
+
+def build(force: bool = False) -> str:
+    """Compile moe_oracle.c into oracle/_build/liboracle.so (host compiler)."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    stale = (not os.path.exists(_LIB_PATH)
+             or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
+    if force or stale:
+        tmp = _LIB_PATH + f".{os.getpid()}.tmp"
+        cc = os.environ.get("CC", "cc")
+        subprocess.run([cc, *CFLAGS, "-o", tmp, _SRC, "-lm"], check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P = ctypes.c_void_p
+            i32 = ctypes.c_int32
+            lib.oracle_bf16_to_f32.argtypes = [ctypes.c_uint16]
+            lib.oracle_bf16_to_f32.restype = ctypes.c_float
+            lib.oracle_f32_to_bf16.argtypes = [ctypes.c_float]
+            lib.oracle_f32_to_bf16.restype = ctypes.c_uint16
+            lib.oracle_e4m3_to_f32.argtypes = [ctypes.c_uint8]
+            lib.oracle_e4m3_to_f32.restype = ctypes.c_float
+            lib.oracle_f32_to_e4m3_satfinite.argtypes = [ctypes.c_float]
+            lib.oracle_f32_to_e4m3_satfinite.restype = ctypes.c_uint8
+            lib.oracle_f32_to_bf16_n.argtypes = [P, ctypes.c_int64, P]
+            lib.oracle_f32_to_bf16_n.restype = None
+            lib.oracle_f32_to_e4m3_n.argtypes = [P, ctypes.c_int64, P]
+            lib.oracle_f32_to_e4m3_n.restype = None
+            lib.oracle_layout.argtypes = [P, i32, i32, i32, i32, P, P, P, P, P]
+            lib.oracle_layout.restype = ctypes.c_uint32
+            lib.oracle_dispatch_bf16.argtypes = [P, i32, i32, i32, P, P]
+            lib.oracle_dispatch_bf16.restype = None
+            lib.oracle_dispatch_fp8.argtypes = [P, i32, i32, i32, P, P, P]
+            lib.oracle_dispatch_fp8.restype = None
+            lib.oracle_combine.argtypes = [P, P, P, i32, i32, i32, P]
+            lib.oracle_combine.restype = None
+            _lib = lib
+    return _lib
+
+
+def _ptr(a: np.ndarray) -> int:
+    assert a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data
+
+
+def _c(a, dtype) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+# --- codecs (scalar; vectorised by numpy.vectorize for the tests) ----------
+
+def bf16_to_f32(h: int) -> float:
+    return float(_load().oracle_bf16_to_f32(int(h)))
+
+
+def f32_to_bf16(f: float) -> int:
+    return int(_load().oracle_f32_to_bf16(float(np.float32(f))))
+
+
+def e4m3_to_f32(c: int) -> float:
+    return float(_load().oracle_e4m3_to_f32(int(c)))
+
+
+def f32_to_e4m3(f: float) -> int:
+    return int(_load().oracle_f32_to_e4m3_satfinite(float(np.float32(f))))
+
+
+def f32_to_bf16_array(a: np.ndarray) -> np.ndarray:
+    a = _c(a, np.float32).ravel()
+    out = np.empty(a.size, np.uint16)
+    _load().oracle_f32_to_bf16_n(_ptr(a), a.size, _ptr(out))
+    return out
+
+
+def f32_to_e4m3_array(a: np.ndarray) -> np.ndarray:
+    a = _c(a, np.float32).ravel()
+    out = np.empty(a.size, np.uint8)
+    _load().oracle_f32_to_e4m3_n(_ptr(a), a.size, _ptr(out))
+    return out
+
+
+# --- the path ---------------------------------------------------------------
+
+class Layout:
+    """Outputs of the layout step (all int32 numpy arrays) plus error bits."""
+
+    def __init__(self, counts, offsets, rank_offsets, src_token, dst_row, error):
+        self.expert_counts = counts
+        self.expert_offsets = offsets
+        self.rank_offsets = rank_offsets
+        self.src_token = src_token
+        self.dst_row = dst_row
+        self.error = int(error)
+
+
+def layout(topk_ids: np.ndarray, E: int, R: int) -> Layout:
+    """Per-expert counts, offsets, rank offsets and the stable slot map.
+
+    ``topk_ids`` is [T, K] int32.  ``src_token`` rows at or beyond
+    ``expert_offsets[E]`` are -1 here (the C code leaves them untouched)."""
+    ids = _c(topk_ids, np.int32)
+    T, K = ids.shape
+    if R <= 0 or E % R != 0:
+        raise ValueError("E must be a positive multiple of R")
+    counts = np.zeros(E, np.int32)
+    offsets = np.zeros(E + 1, np.int32)
+    rank_offsets = np.zeros(R + 1, np.int32)
+    src_token = np.full(max(T * K, 1), -1, np.int32)[: T * K].copy()
+    dst_row = np.zeros((T, K), np.int32)
+    err = _load().oracle_layout(_ptr(ids), T, K, E, R, _ptr(counts),
+                                _ptr(offsets), _ptr(rank_offsets),
+                                _ptr(src_token), _ptr(dst_row))
+    return Layout(counts, offsets, rank_offsets, src_token, dst_row, err)
+
+
+def dispatch_bf16(tokens_bits: np.ndarray, dst_row: np.ndarray) -> np.ndarray:
+    """packed[dst_row[t,k]] = tokens[t]; bf16 carried as uint16 bit patterns."""
+    x = _c(tokens_bits, np.uint16)
+    T, H = x.shape
+    d = _c(dst_row, np.int32)
+    K = d.shape[1]
+    packed = np.zeros((T * K, H), np.uint16)
+    _load().oracle_dispatch_bf16(_ptr(x), T, H, K, _ptr(d), _ptr(packed))
+    return packed
+
+
+def dispatch_fp8(tokens_bits: np.ndarray, dst_row: np.ndarray):
+    """Block-scaled e4m3 dispatch; returns (codes uint8 [T*K,H], scales f32 [T*K,H/128])."""
+    x = _c(tokens_bits, np.uint16)
+    T, H = x.shape
+    if H % 128:
+        raise ValueError("H must be a multiple of 128 for FP8 dispatch")
+    d = _c(dst_row, np.int32)
+    K = d.shape[1]
+    codes = np.zeros((T * K, H), np.uint8)
+    scales = np.zeros((T * K, H // 128), np.float32)
+    _load().oracle_dispatch_fp8(_ptr(x), T, H, K, _ptr(d), _ptr(codes),
+                                _ptr(scales))
+    return codes, scales
+
+
+def combine(y_bits: np.ndarray, topk_weights: np.ndarray,
+            dst_row: np.ndarray) -> np.ndarray:
+    """out[t] = bf16(sum_k w[t,k] * y[dst_row[t,k]]) as an fp32 FMA chain in k order."""
+    y = _c(y_bits, np.uint16)
+    w = _c(topk_weights, np.float32)
+    d = _c(dst_row, np.int32)
+    T, K = d.shape
+    H = y.shape[1]
+    out = np.zeros((T, H), np.uint16)
+    _load().oracle_combine(_ptr(y), _ptr(w), _ptr(d), T, H, K, _ptr(out))
+    return out

@@ -1,0 +1,246 @@
+"""Pins for the oracle's dispatch (bf16 and block-scaled FP8) and combine.
+
+* bf16 dispatch: bit identity of every packed row with its source row.
+* FP8 dispatch: each code is the nearest e4m3 value of x/scale found by
+  exhaustive search over the code table (ties to the even code, saturating);
+  the dequantisation error obeys the closed-form bound of the block scale; the
+  block's largest element decodes to exactly +-448 * scale.
+* combine: exact rational arithmetic (Python fractions) of the defined fp32
+  fused-multiply-add chain, including cases built so that a separate
+  multiply and add, another k order or a non-zero start would differ; the
+  identity round trip combine(dispatch(x)) == x; the closed form
+  sum_k w_k * s_e * x for per-expert-scalar experts.
+"""
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+from combine_moe_layout_05_gb300 import workload as wl
+
+
+def f32(bits_u16):
+    return wl.bf16_bits_to_f32(bits_u16)
+
+
+# ---------------------------------------------------------------- dispatch --
+
+@pytest.mark.parametrize("name", ["tiny", "decode_dsv3", "prefill_kimi_k2"])
+def test_dispatch_bf16_bit_identity(oracle, name):
+    w = wl.get(name)
+    inp = wl.make_inputs(w, T=min(w.T, 512))
+    lay = oracle.layout(inp.topk_ids, w.E, w.R)
+    packed = oracle.dispatch_bf16(inp.tokens, lay.dst_row)
+    assert np.array_equal(packed, inp.tokens[lay.src_token])
+    for t in range(0, inp.tokens.shape[0], 37):
+        for k in range(w.K):
+            assert np.array_equal(packed[lay.dst_row[t, k]], inp.tokens[t])
+
+
+def _e4m3_table():
+    v = torch.from_numpy(np.arange(128, dtype=np.uint8)).view(
+        torch.float8_e4m3fn).float().numpy().astype(np.float64)
+    return v[:127]
+
+
+def _nearest_even_code(v_abs):
+    table = _e4m3_table()
+    codes = np.arange(127)[None, :]
+    out = np.empty(v_abs.size, np.int64)
+    for s in range(0, v_abs.size, 32768):
+        a = np.minimum(v_abs[s:s + 32768], 448.0)
+        d = np.abs(a[:, None] - table[None, :])
+        cand = d == d.min(axis=1, keepdims=True)
+        tie = cand.sum(axis=1) > 1
+        even = np.where(cand & (codes % 2 == 0), codes, 999).min(axis=1)
+        first = np.where(cand, codes, 999).min(axis=1)
+        out[s:s + 32768] = np.where(tie, even, first)
+    return out
+
+
+@pytest.mark.parametrize("name,T", [("tiny", 64), ("decode_dsv3_fp8", 16),
+                                    ("prefill_qwen3", 40)])
+def test_dispatch_fp8_codes_by_search_and_bound(oracle, name, T):
+    w = wl.get(name)
+    inp = wl.make_inputs(w, T=T)
+    # plant zero blocks (with signed zeros) and a denormal-only block
+    x_bits = inp.tokens.copy()
+    x_bits[0, :128] = 0
+    x_bits[0, 3] = 0x8000
+    if T > 1:
+        x_bits[1, 128:256] = 0x0001          # smallest bf16 subnormal
+    lay = oracle.layout(inp.topk_ids, w.E, w.R)
+    codes, scales = oracle.dispatch_fp8(x_bits, lay.dst_row)
+    H, nb = w.H, w.H // 128
+    x = f32(x_bits).reshape(T, nb, 128)
+    amax = np.abs(x).max(axis=2)
+    scale = (amax / np.float32(448.0)).astype(np.float32)
+    # every slot of a token carries the same codes and scales
+    src = lay.src_token
+    got_codes = codes.reshape(T * w.K, nb, 128)
+    got_scales = scales
+    assert np.array_equal(got_scales.view(np.uint32), scale[src].view(np.uint32))
+
+    v = np.zeros_like(x)
+    nz = amax > 0
+    with np.errstate(divide="ignore", invalid="ignore"):
+        v = np.where(nz[:, :, None], x / scale[:, :, None], x)   # fp32 divide
+    exp_mag = _nearest_even_code(np.abs(v.astype(np.float64)).ravel())
+    exp_mag = np.where(nz[:, :, None].repeat(128, 2).ravel(), exp_mag, 0)
+    exp = (exp_mag | (np.signbit(v.ravel()).astype(np.int64) << 7)).astype(np.uint8)
+    exp = exp.reshape(T, nb, 128)
+    assert np.array_equal(got_codes, exp[src])
+
+    # closed-form bound: |x - q*scale| <= scale * (half spacing at |x/scale|)
+    # + |x| * 2^-23 (the rounding of x/scale itself), which is <= amax/28
+    q = torch.from_numpy(got_codes.reshape(-1)).view(torch.float8_e4m3fn).float().numpy()
+    q = q.reshape(T * w.K, nb, 128).astype(np.float64)
+    deq = q * got_scales[:, :, None].astype(np.float64)
+    xs = x[src].astype(np.float64)
+    err = np.abs(xs - deq)
+    sc = got_scales[:, :, None].astype(np.float64)
+    vabs = np.abs(xs) / np.maximum(sc, 1e-300)
+    e = np.floor(np.log2(np.maximum(vabs, 2.0 ** -6)))
+    half = np.exp2(e - 4)
+    bound = sc * half * (1 + 2.0 ** -20) + np.abs(xs) * 2.0 ** -23
+    assert np.all(err <= bound + 1e-300)
+    amax_s = amax[src].astype(np.float64)
+    assert np.all(err <= amax_s[:, :, None] / 28 * (1 + 2.0 ** -20))
+    # the element holding amax decodes to +-448 * scale exactly
+    idx = np.argmax(np.abs(xs), axis=2)
+    qa = np.take_along_axis(q, idx[:, :, None], 2)[:, :, 0]
+    big = amax_s > 0
+    assert np.all(np.abs(qa[big]) == 448.0)
+
+
+# ----------------------------------------------------------------- combine --
+
+def _round_fraction(q: Fraction, mant_bits: int) -> Fraction:
+    """Round a rational to the nearest binary float with `mant_bits` fraction
+    bits and fp32's exponent range, ties to even (no overflow here)."""
+    if q == 0:
+        return Fraction(0)
+    s = -1 if q < 0 else 1
+    a = abs(q)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    if Fraction(2) ** e > a:
+        e -= 1
+    e = max(e, -126)
+    step = Fraction(2) ** (e - mant_bits)
+    n = a / step
+    fl = n.numerator // n.denominator
+    rem = n - fl
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and fl % 2 == 1):
+        fl += 1
+    return s * fl * step
+
+
+def exact_combine(y_bits, w, dst_row):
+    """The defined combine in exact arithmetic: acc starts at +0, each step
+    rounds w*y + acc once to fp32, the end result rounds once to bf16."""
+    T, K = dst_row.shape
+    H = y_bits.shape[1]
+    yf = f32(y_bits)
+    out = np.zeros((T, H), np.uint16)
+    for t in range(T):
+        for j in range(H):
+            acc = Fraction(0)
+            for k in range(K):
+                r = dst_row[t, k]
+                acc = _round_fraction(Fraction(float(w[t, k])) * Fraction(float(yf[r, j])) + acc, 23)
+            b = _round_fraction(acc, 7)
+            out[t, j] = wl.to_bf16_bits(np.array([float(b)], np.float32))[0]
+            if b == 0:
+                out[t, j] = 0            # +0: the chain starts at +0
+    return out
+
+
+def test_combine_exact_rational_random(oracle):
+    rng = np.random.default_rng(3)
+    for trial in range(6):
+        T, H, K = 3, 8, (1, 2, 3, 4, 8, 5)[trial]
+        y = wl.to_bf16_bits((rng.standard_normal((T * K, H)) *
+                             np.exp2(rng.integers(-20, 20, (T * K, H)))).astype(np.float32))
+        w = (rng.standard_normal((T, K)) * np.exp2(rng.integers(-8, 8, (T, K)))).astype(np.float32)
+        dst = rng.permutation(T * K).astype(np.int32).reshape(T, K)
+        got = oracle.combine(y, w, dst)
+        assert np.array_equal(got, exact_combine(y, w, dst)), trial
+
+
+def test_combine_exact_rational_fma_sensitive(oracle):
+    """w0*y0 + w1*y1 with y1 = -y0: the fused chain leaves exactly the
+    rounding error of w0*y0; a separate multiply and add would give 0."""
+    w0 = np.float32(1 + 2.0 ** -23)
+    y0 = np.float32(1 - 2.0 ** -8)
+    y = wl.to_bf16_bits(np.array([[y0] * 8, [-y0] * 8], np.float32))
+    w = np.array([[w0, w0]], np.float32)
+    dst = np.array([[0, 1]], np.int32)
+    got = oracle.combine(y, w, dst)
+    exp = exact_combine(y, w, dst)
+    assert np.array_equal(got, exp)
+    assert np.all(f32(got) != 0)          # nonzero only with a fused chain
+    # order matters: a large term first then cancelling small terms
+    y2 = wl.to_bf16_bits(np.array([[2.0 ** 30] * 8, [1.0] * 8, [-(2.0 ** 30)] * 8],
+                                  np.float32))
+    w2 = np.array([[1.0, 1.0, 1.0]], np.float32)
+    d2 = np.array([[0, 1, 2]], np.int32)
+    got2 = oracle.combine(y2, w2, d2)
+    assert np.array_equal(got2, exact_combine(y2, w2, d2))
+    assert np.all(got2 == 0)              # 2^30 + 1 rounds to 2^30 in fp32
+    d3 = np.array([[0, 2, 1]], np.int32)  # other order: exact 1.0
+    got3 = oracle.combine(y2, w2, d3)
+    assert np.all(f32(got3) == 1.0)
+
+
+def test_combine_signed_zero_start(oracle):
+    """All terms -0: a chain starting at +0 ends at +0."""
+    y = np.full((2, 8), 0x8000, np.uint16)
+    w = np.array([[1.0, 1.0]], np.float32)
+    got = oracle.combine(y, w, np.array([[0, 1]], np.int32))
+    assert np.all(got == 0x0000)
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode_dsv3", "prefill_qwen3"])
+def test_identity_round_trip(oracle, name):
+    """combine(dispatch(x)) with identity experts and weights summing to one
+    returns x: the fp32 sum is within K*2^-24 relative of x, far inside half a
+    bf16 step, so rounding lands back on x."""
+    w = wl.get(name)
+    inp = wl.make_inputs(w, T=min(w.T, 256))
+    lay = oracle.layout(inp.topk_ids, w.E, w.R)
+    packed = oracle.dispatch_bf16(inp.tokens, lay.dst_row)
+    out = oracle.combine(packed, inp.topk_weights, lay.dst_row)
+    # equal as numbers; a -0 input comes back as +0 (the chain starts at +0)
+    assert np.array_equal(f32(out), f32(inp.tokens))
+    nz = f32(inp.tokens) != 0
+    assert np.array_equal(out[nz], inp.tokens[nz])
+
+
+def test_identity_single_expert(oracle):
+    rng = np.random.default_rng(9)
+    x = wl.to_bf16_bits(rng.standard_normal((32, 64)).astype(np.float32))
+    ids = rng.integers(0, 4, (32, 1)).astype(np.int32)
+    lay = oracle.layout(ids, 4, 2)
+    packed = oracle.dispatch_bf16(x, lay.dst_row)
+    out = oracle.combine(packed, np.ones((32, 1), np.float32), lay.dst_row)
+    assert np.array_equal(out, x)
+
+
+def test_per_expert_scalar_closed_form(oracle):
+    """y = bf16(x * s_e): out matches sum_k w_k * y_k (exact in fp64) within
+    the fp32 chain's error and one bf16 rounding."""
+    w = wl.get("decode_dsv3")
+    inp = wl.make_inputs(w, T=32)
+    lay = oracle.layout(inp.topk_ids, w.E, w.R)
+    packed = oracle.dispatch_bf16(inp.tokens, lay.dst_row)
+    e_of_row = np.searchsorted(lay.expert_offsets[1:], np.arange(32 * w.K), side="right")
+    y = wl.to_bf16_bits(f32(packed) * inp.expert_scale[e_of_row][:, None])
+    out = oracle.combine(y, inp.topk_weights, lay.dst_row)
+    yd = f32(y).astype(np.float64)
+    exact = np.einsum("tk,tkh->th", inp.topk_weights.astype(np.float64),
+                      yd[lay.dst_row])
+    mag = np.einsum("tk,tkh->th", np.abs(inp.topk_weights.astype(np.float64)),
+                    np.abs(yd[lay.dst_row]))
+    err = np.abs(f32(out).astype(np.float64) - exact)
+    assert np.all(err <= np.abs(exact) * 2.0 ** -8 + mag * w.K * 2.0 ** -23 + 1e-30)
