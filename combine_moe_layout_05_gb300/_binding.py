@@ -1,0 +1,187 @@
+"""Thin ctypes binding over libmoe_layout.so (argument marshalling only).
+
+Every function has the name of its C entry point and forwards raw device
+pointers, sizes and the current CUDA stream; all computation happens in the
+library's CUDA kernels.  There is no CPU fallback: if the library is missing
+or a call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+
+import torch
+
+from . import build as _build
+
+MOE_OK = 0
+MOE_DEV_ERR_EXPERT_RANGE = 1
+MOE_DEV_ERR_DUPLICATE = 2
+
+_lock = threading.Lock()
+_lib = None
+
+
+class MoeError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} failed: {moe_status_string(status)} (status {status})")
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load(path: str | None = None):
+    """Load the CUDA library (built beforehand by build.build())."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            p = path or _build.LIB_PATH
+            if not os.path.exists(p):
+                raise RuntimeError(
+                    f"{p} is missing: build it with "
+                    "combine_moe_layout_05_gb300.build.build()")
+            lib = ctypes.CDLL(p)
+            P, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+            lib.moe_status_string.argtypes = [ctypes.c_int]
+            lib.moe_status_string.restype = ctypes.c_char_p
+            lib.moe_layout_workspace_bytes.argtypes = [i32, i32, i32]
+            lib.moe_layout_workspace_bytes.restype = sz
+            lib.moe_layout.argtypes = [P, i32, i32, i32, i32, P, P, P, P, P, P,
+                                       P, sz, P]
+            lib.moe_layout.restype = ctypes.c_int
+            lib.moe_dispatch.argtypes = [P, i32, i32, i32, P, i32, P, P, P]
+            lib.moe_dispatch.restype = ctypes.c_int
+            lib.moe_combine.argtypes = [P, P, P, i32, i32, i32, P, P]
+            lib.moe_combine.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def declared_functions(header: str | None = None) -> list[str]:
+    """Names of the functions the public header declares."""
+    header = header or os.path.join(_build.INCLUDE, "moe_layout.h")
+    text = open(header).read()
+    return sorted(set(re.findall(r"MOE_API\s+[\w\s\*]*?\b(moe_\w+)\s*\(", text)))
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    return t.data_ptr() if t.numel() > 0 else None
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check(name: str, t, dtype, device=None):
+    if t is None:
+        return
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.numel() and not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+
+
+def _raise(fn: str, status: int):
+    if status != MOE_OK:
+        raise MoeError(fn, status)
+
+
+def moe_status_string(status: int) -> str:
+    return load().moe_status_string(int(status)).decode()
+
+
+def moe_layout_workspace_bytes(T: int, K: int, E: int) -> int:
+    return int(load().moe_layout_workspace_bytes(T, K, E))
+
+
+def moe_layout(topk_ids, E: int, R: int, expert_counts, expert_offsets,
+               rank_offsets, src_token, dst_row, dev_error=None,
+               workspace=None, stream=None) -> None:
+    """Routing histogram, scan and stable slot map (see include/moe_layout.h)."""
+    T, K = topk_ids.shape
+    _check("topk_ids", topk_ids, torch.int32)
+    for n, t in (("expert_counts", expert_counts), ("expert_offsets", expert_offsets),
+                 ("rank_offsets", rank_offsets), ("src_token", src_token),
+                 ("dst_row", dst_row)):
+        _check(n, t, torch.int32)
+    if expert_counts.numel() < E or expert_offsets.numel() < E + 1 or rank_offsets.numel() < R + 1:
+        raise ValueError("moe_layout: output arrays too small")
+    if src_token.numel() < T * K or dst_row.numel() < T * K:
+        raise ValueError("moe_layout: src_token/dst_row too small")
+    if dev_error is not None:
+        _check("dev_error", dev_error, torch.int32)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = load().moe_layout(_ptr(topk_ids), T, K, E, R, _ptr(expert_counts),
+                           _ptr(expert_offsets), _ptr(rank_offsets),
+                           _ptr(src_token), _ptr(dst_row), _ptr(dev_error),
+                           _ptr(workspace), ws_bytes, _stream(stream))
+    _raise("moe_layout", st)
+
+
+def moe_dispatch(tokens, dst_row, packed, scales=None, fp8: bool = False,
+                 stream=None) -> None:
+    """Pack token rows into their K slots, bf16 or block-scaled e4m3."""
+    T, H = tokens.shape
+    K = dst_row.shape[1] if dst_row.dim() == 2 else 1
+    _check("tokens", tokens, torch.bfloat16)
+    _check("dst_row", dst_row, torch.int32)
+    if fp8:
+        _check("packed", packed, torch.float8_e4m3fn)
+        _check("scales", scales, torch.float32)
+        if scales is None or scales.numel() < T * K * (H // 128):
+            raise ValueError("moe_dispatch: scales missing or too small")
+    else:
+        _check("packed", packed, torch.bfloat16)
+    if dst_row.numel() != T * K or packed.numel() < T * K * H:
+        raise ValueError("moe_dispatch: dst_row/packed have the wrong size")
+    st = load().moe_dispatch(_ptr(tokens), T, H, K, _ptr(dst_row), int(bool(fp8)),
+                             _ptr(packed), _ptr(scales) if fp8 else None,
+                             _stream(stream))
+    _raise("moe_dispatch", st)
+
+
+def moe_combine(expert_out, topk_weights, dst_row, out, stream=None) -> None:
+    """Routing-weighted fp32 sum of each token's K expert rows, rounded to bf16."""
+    T, K = topk_weights.shape
+    H = out.shape[1]
+    _check("expert_out", expert_out, torch.bfloat16)
+    _check("topk_weights", topk_weights, torch.float32)
+    _check("dst_row", dst_row, torch.int32)
+    _check("out", out, torch.bfloat16)
+    if dst_row.numel() != T * K or out.shape[0] != T or expert_out.numel() < T * K * H:
+        raise ValueError("moe_combine: argument sizes disagree")
+    st = load().moe_combine(_ptr(expert_out), _ptr(topk_weights), _ptr(dst_row),
+                            T, H, K, _ptr(out), _stream(stream))
+    _raise("moe_combine", st)
+
+
+class LayoutBuffers:
+    """Device buffers for one layout of T x K entries (allocated by torch)."""
+
+    def __init__(self, T: int, K: int, E: int, R: int, device="cuda"):
+        i32 = dict(dtype=torch.int32, device=device)
+        self.T, self.K, self.E, self.R = T, K, E, R
+        self.expert_counts = torch.empty(E, **i32)
+        self.expert_offsets = torch.empty(E + 1, **i32)
+        self.rank_offsets = torch.empty(R + 1, **i32)
+        self.src_token = torch.empty(T * K, **i32)
+        self.dst_row = torch.empty((T, K), **i32)
+        self.dev_error = torch.empty(1, **i32)
+        ws = moe_layout_workspace_bytes(T, K, E)
+        self.workspace = torch.empty(ws, dtype=torch.uint8, device=device) if ws else None
+
+    def run(self, topk_ids, stream=None) -> "LayoutBuffers":
+        moe_layout(topk_ids, self.E, self.R, self.expert_counts,
+                   self.expert_offsets, self.rank_offsets, self.src_token,
+                   self.dst_row, self.dev_error, self.workspace, stream)
+        return self

@@ -1,0 +1,110 @@
+// api.cu -- the C ABI: host-side argument checks, then the launchers.
+// Nothing here allocates memory or synchronises a stream.
+#include "internal.h"
+#include "moe_layout.h"
+
+#include <cstdint>
+
+namespace {
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+bool layout_sizes_ok(int32_t T, int32_t K, int32_t E)
+{
+    if (T < 0 || E < 1 || E > MOE_MAX_EXPERTS) return false;
+    if (K < 1 || K > MOE_MAX_TOPK || K > E) return false;
+    return (int64_t)T * K <= (int64_t)INT32_MAX - 1;
+}
+
+moe_status_t rows_ok(int32_t T, int32_t H, int32_t K)
+{
+    if (T < 0 || K < 1 || K > MOE_MAX_TOPK || H < 8 || H % 8 != 0) return MOE_ERR_INVALID_ARG;
+    if ((int64_t)T * K > (int64_t)INT32_MAX - 1) return MOE_ERR_INVALID_ARG;
+    return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *moe_status_string(moe_status_t status)
+{
+    switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_ALIGNMENT: return "misaligned pointer";
+    case MOE_ERR_CUDA: return "CUDA launch failed";
+    case MOE_ERR_WORKSPACE: return "workspace missing or too small";
+    }
+    return "unknown status";
+}
+
+size_t moe_layout_workspace_bytes(int32_t T, int32_t K, int32_t E)
+{
+    if (!layout_sizes_ok(T, K, E)) return 0;
+    return moe::layout_workspace_bytes(moe::plan_layout(T, K, E), E);
+}
+
+moe_status_t moe_layout(const int32_t *topk_ids, int32_t T, int32_t K,
+                        int32_t E, int32_t R, int32_t *expert_counts,
+                        int32_t *expert_offsets, int32_t *rank_offsets,
+                        int32_t *src_token, int32_t *dst_row,
+                        uint32_t *dev_error, void *workspace,
+                        size_t workspace_bytes, cudaStream_t stream)
+{
+    if (!layout_sizes_ok(T, K, E) || R < 1 || E % R != 0) return MOE_ERR_INVALID_ARG;
+    if (!expert_counts || !expert_offsets || !rank_offsets) return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (!topk_ids || !src_token || !dst_row)) return MOE_ERR_INVALID_ARG;
+    const void *p4[] = {topk_ids, expert_counts, expert_offsets, rank_offsets,
+                        src_token, dst_row, dev_error};
+    for (const void *p : p4)
+        if (!aligned(p, 4)) return MOE_ERR_ALIGNMENT;
+    const size_t need = moe::layout_workspace_bytes(moe::plan_layout(T, K, E), E);
+    if (need > 0) {
+        if (!workspace || workspace_bytes < need) return MOE_ERR_WORKSPACE;
+        if (!aligned(workspace, 16)) return MOE_ERR_ALIGNMENT;
+    }
+    return cuda_status(moe::launch_layout(topk_ids, T, K, E, R, expert_counts,
+                                          expert_offsets, rank_offsets,
+                                          src_token, dst_row, dev_error,
+                                          workspace, stream));
+}
+
+moe_status_t moe_dispatch(const void *tokens, int32_t T, int32_t H, int32_t K,
+                          const int32_t *dst_row, int32_t fp8, void *packed,
+                          float *scales, cudaStream_t stream)
+{
+    moe_status_t s = rows_ok(T, H, K);
+    if (s != MOE_OK) return s;
+    if (fp8 != 0 && fp8 != 1) return MOE_ERR_INVALID_ARG;
+    if (fp8 && H % 128 != 0) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;
+    if (!tokens || !dst_row || !packed || (fp8 && !scales)) return MOE_ERR_INVALID_ARG;
+    if (!aligned(tokens, 16) || !aligned(packed, 16) || !aligned(dst_row, 4) ||
+        (fp8 && !aligned(scales, 4)))
+        return MOE_ERR_ALIGNMENT;
+    if (fp8)
+        return cuda_status(moe::launch_dispatch_fp8(tokens, T, H, K, dst_row,
+                                                    packed, scales, stream));
+    return cuda_status(moe::launch_dispatch_bf16(tokens, T, H, K, dst_row,
+                                                 packed, stream));
+}
+
+moe_status_t moe_combine(const void *expert_out, const float *topk_weights,
+                         const int32_t *dst_row, int32_t T, int32_t H,
+                         int32_t K, void *out, cudaStream_t stream)
+{
+    moe_status_t s = rows_ok(T, H, K);
+    if (s != MOE_OK) return s;
+    if (T == 0) return MOE_OK;
+    if (!expert_out || !topk_weights || !dst_row || !out) return MOE_ERR_INVALID_ARG;
+    if (!aligned(expert_out, 16) || !aligned(out, 16) || !aligned(topk_weights, 4) ||
+        !aligned(dst_row, 4))
+        return MOE_ERR_ALIGNMENT;
+    return cuda_status(moe::launch_combine(expert_out, topk_weights, dst_row, T,
+                                           H, K, out, stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,43 @@
+// internal.h -- launchers shared between the C-ABI layer and the kernels.
+// Every launcher assumes its arguments have already been validated.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace moe {
+
+// How the layout of T*K entries is split over thread blocks.
+struct LayoutPlan {
+    bool fused;            // one block does everything (no workspace)
+    int tokens_per_chunk;  // tokens per block in the multi-block path
+    int chunks;            // number of blocks in the multi-block path
+};
+
+LayoutPlan plan_layout(int T, int K, int E);
+size_t layout_workspace_bytes(const LayoutPlan &plan, int E);
+
+cudaError_t launch_layout(const int32_t *topk_ids, int T, int K, int E, int R,
+                          int32_t *expert_counts, int32_t *expert_offsets,
+                          int32_t *rank_offsets, int32_t *src_token,
+                          int32_t *dst_row, uint32_t *dev_error,
+                          void *workspace, cudaStream_t stream);
+
+cudaError_t launch_dispatch_bf16(const void *tokens, int T, int H, int K,
+                                 const int32_t *dst_row, void *packed,
+                                 cudaStream_t stream);
+
+cudaError_t launch_dispatch_fp8(const void *tokens, int T, int H, int K,
+                                const int32_t *dst_row, void *packed,
+                                float *scales, cudaStream_t stream);
+
+cudaError_t launch_combine(const void *expert_out, const float *topk_weights,
+                           const int32_t *dst_row, int T, int H, int K,
+                           void *out, cudaStream_t stream);
+
+// Threads per block for `units` work items per row: the largest multiple of
+// 32 up to 256 that divides `units`, else 128 (last block of a row partial).
+int pick_row_block(int units);
+
+}  // namespace moe

@@ -35,6 +35,12 @@
 #include <stdint.h>
 #include <cuda_runtime_api.h>
 
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -58,12 +64,12 @@ typedef enum moe_status {
 #define MOE_MAX_TOPK 32
 
 /* Human-readable name of a status code (static storage, never NULL). */
-const char *moe_status_string(moe_status_t status);
+MOE_API const char *moe_status_string(moe_status_t status);
 
 /* Bytes of device workspace moe_layout needs for these sizes (0 when the
  * whole layout fits one thread block).  Returns 0 for invalid sizes, which
  * moe_layout then rejects. */
-size_t moe_layout_workspace_bytes(int32_t T, int32_t K, int32_t E);
+MOE_API size_t moe_layout_workspace_bytes(int32_t T, int32_t K, int32_t E);
 
 /*
  * moe_layout -- routing histogram, exclusive scan and stable slot map.
@@ -104,7 +110,7 @@ size_t moe_layout_workspace_bytes(int32_t T, int32_t K, int32_t E);
  *              stream passes this call.
  * T == 0 writes zero counts and offsets.
  */
-moe_status_t moe_layout(const int32_t *topk_ids, int32_t T, int32_t K,
+MOE_API moe_status_t moe_layout(const int32_t *topk_ids, int32_t T, int32_t K,
                         int32_t E, int32_t R,
                         int32_t *expert_counts, int32_t *expert_offsets,
                         int32_t *rank_offsets, int32_t *src_token,
@@ -137,7 +143,7 @@ moe_status_t moe_layout(const int32_t *topk_ids, int32_t T, int32_t K,
  *          ignored otherwise.
  * H >= 8 with H % 8 == 0 (H % 128 == 0 when fp8 == 1).  T == 0 is a no-op.
  */
-moe_status_t moe_dispatch(const void *tokens, int32_t T, int32_t H, int32_t K,
+MOE_API moe_status_t moe_dispatch(const void *tokens, int32_t T, int32_t H, int32_t K,
                           const int32_t *dst_row, int32_t fp8, void *packed,
                           float *scales, cudaStream_t stream);
 
@@ -161,7 +167,7 @@ moe_status_t moe_dispatch(const void *tokens, int32_t T, int32_t H, int32_t K,
  * out           [T,H] bf16, 16-byte aligned; must not overlap expert_out.
  * H >= 8 with H % 8 == 0.  T == 0 is a no-op.
  */
-moe_status_t moe_combine(const void *expert_out, const float *topk_weights,
+MOE_API moe_status_t moe_combine(const void *expert_out, const float *topk_weights,
                          const int32_t *dst_row, int32_t T, int32_t H,
                          int32_t K, void *out, cudaStream_t stream);
 

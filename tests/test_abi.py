@@ -1,0 +1,94 @@
+"""The C-ABI library builds for sm_103a, loads, exports every function the
+public header declares, and rejects bad arguments on the host before touching
+a GPU (these checks return before any CUDA call, so they run without one)."""
+import ctypes
+import os
+
+import pytest
+
+import combine_moe_layout_05_gb300 as moe
+from combine_moe_layout_05_gb300 import build as moe_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    moe_build.build()
+    return moe.load()
+
+
+def test_header_declares_the_boundary():
+    names = moe.declared_functions()
+    for n in ["moe_layout", "moe_dispatch", "moe_combine",
+              "moe_layout_workspace_bytes", "moe_status_string"]:
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if h.endswith(".h"):
+            for name in moe.declared_functions(os.path.join(ROOT, "include", h)):
+                assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    assert moe.moe_status_string(0) == "ok"
+    assert "alignment" in moe.moe_status_string(2) or "misaligned" in moe.moe_status_string(2)
+    assert moe.moe_status_string(99) == "unknown status"
+
+
+def test_workspace_query(lib):
+    assert moe.moe_layout_workspace_bytes(128, 8, 256) == 0          # one block
+    ws = moe.moe_layout_workspace_bytes(16384, 8, 128)
+    assert ws > 0 and ws % 256 == 0
+    assert moe.moe_layout_workspace_bytes(16384, 8, 100000) == 0     # invalid E
+
+
+# Fake, never-dereferenced device addresses: the host checks reject the call
+# before anything is launched.
+FAKE = 0x10000
+P = ctypes.c_void_p
+
+
+def _layout(lib, ids=FAKE, T=4, K=2, E=8, R=2, outs=FAKE, ws=None, wsb=0):
+    return lib.moe_layout(P(ids), T, K, E, R, P(outs), P(outs), P(outs),
+                          P(outs), P(outs), None, P(ws) if ws else None, wsb, None)
+
+
+def test_layout_host_checks(lib):
+    assert _layout(lib, E=8, R=3) == 1            # E % R != 0
+    assert _layout(lib, K=9, E=8) == 1            # K > E
+    assert _layout(lib, K=33, E=64) == 1          # K > MOE_MAX_TOPK
+    assert _layout(lib, E=2048, R=2) == 1         # E > MOE_MAX_EXPERTS
+    assert _layout(lib, T=-1) == 1
+    assert _layout(lib, ids=0) == 1               # null ids with T > 0
+    assert _layout(lib, outs=0) == 1
+    assert _layout(lib, ids=FAKE + 2) == 2        # misaligned
+    assert _layout(lib, T=100000, K=8, E=128, R=16) == 4   # workspace missing
+    need = moe.moe_layout_workspace_bytes(100000, 8, 128)
+    assert _layout(lib, T=100000, K=8, E=128, R=16, ws=FAKE, wsb=need - 1) == 4
+    assert _layout(lib, T=100000, K=8, E=128, R=16, ws=FAKE + 8, wsb=need) == 2
+    assert _layout(lib, T=2**28, K=16, E=64, R=1) == 1     # T*K >= 2^31
+
+
+def test_dispatch_host_checks(lib):
+    d = lib.moe_dispatch
+    assert d(P(FAKE), 4, 100, 2, P(FAKE), 0, P(FAKE), None, None) == 1   # H % 8
+    assert d(P(FAKE), 4, 136, 2, P(FAKE), 1, P(FAKE), P(FAKE), None) == 1  # H % 128 (fp8)
+    assert d(P(FAKE), 4, 128, 2, P(FAKE), 1, P(FAKE), None, None) == 1   # no scales
+    assert d(P(FAKE), 4, 128, 2, P(FAKE), 2, P(FAKE), None, None) == 1   # bad fp8 flag
+    assert d(P(FAKE + 8), 4, 128, 2, P(FAKE), 0, P(FAKE), None, None) == 2
+    assert d(P(FAKE), 4, 128, 2, P(FAKE), 0, P(FAKE + 4), None, None) == 2
+    assert d(None, 4, 128, 2, P(FAKE), 0, P(FAKE), None, None) == 1
+    assert d(None, 0, 128, 2, None, 0, None, None, None) == 0          # T == 0: no-op
+
+
+def test_combine_host_checks(lib):
+    c = lib.moe_combine
+    assert c(P(FAKE), P(FAKE), P(FAKE), 4, 12, 2, P(FAKE), None) == 1    # H % 8
+    assert c(P(FAKE), P(FAKE), P(FAKE), 4, 128, 0, P(FAKE), None) == 1   # K == 0
+    assert c(P(FAKE + 8), P(FAKE), P(FAKE), 4, 128, 2, P(FAKE), None) == 2
+    assert c(P(FAKE), P(FAKE + 2), P(FAKE), 4, 128, 2, P(FAKE), None) == 2
+    assert c(P(FAKE), P(FAKE), None, 4, 128, 2, P(FAKE), None) == 1
+    assert c(None, None, None, 0, 128, 2, None, None) == 0              # T == 0: no-op
