@@ -59,6 +59,8 @@ def parse_args(argv=None):
                    help="host time spent timing the oracle baseline")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--unfused", action="store_true",
+                   help="moe_layout + moe_dispatch as two calls instead of moe_layout_dispatch")
     return p.parse_args(argv)
 
 
@@ -113,13 +115,17 @@ def algorithmic_bytes(w, dispatch: str):
     else:
         disp = 2 * T * H + T * K * H + 4 * T * K * (H // 128) + 4 * T * K
     comb = 2 * T * K * H + 8 * T * K + 2 * T * H
-    return {"layout": layout, "dispatch": disp, "combine": comb}
+    return {"layout": layout, "dispatch": disp, "combine": comb,
+            "layout_dispatch": layout + disp - 4 * T * K}
 
 
 def kernel_source_hash(kernel: str) -> str:
-    src = {"layout": "layout.cu", "dispatch": "dispatch.cu", "combine": "combine.cu"}[kernel]
+    srcs = {"layout": ["layout.cu"], "dispatch": ["dispatch.cu", "rowops.cuh"],
+            "combine": ["combine.cu"],
+            "layout_dispatch": ["layout_dispatch.cu", "rowops.cuh", "layout.cu",
+                                "dispatch.cu"]}[kernel]
     h = hashlib.sha256()
-    for f in (src, "common.cuh"):
+    for f in srcs + ["common.cuh"]:
         with open(os.path.join(ROOT, "combine_moe_layout_05_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:12]
@@ -327,21 +333,23 @@ def expert_outputs(w, dispatch, inp, buf):
     return y.view(torch.int16).cpu().numpy().view("uint16")
 
 
-def run_step(moe, buf, dispatch, ev=None, evs=None, stream_handle=None):
-    if ev is not None:
-        ev.record(evs[0], stream_handle)
-    buf.layout.run(buf.ids)
-    if ev is not None:
-        ev.record(evs[1], stream_handle)
-    if dispatch == "bf16":
-        moe.moe_dispatch(buf.tokens, buf.layout.dst_row, buf.packed)
+def step_ops(moe, dispatch, unfused=False):
+    """The calls of one step, as (name, fn(buffer_set)) in launch order."""
+    fp8 = dispatch == "fp8"
+    if unfused:
+        ops = [("layout", lambda b: b.layout.run(b.ids)),
+               ("dispatch", lambda b: moe.moe_dispatch(b.tokens, b.layout.dst_row,
+                                                       b.packed, b.scales, fp8=fp8))]
     else:
-        moe.moe_dispatch(buf.tokens, buf.layout.dst_row, buf.packed, buf.scales, fp8=True)
-    if ev is not None:
-        ev.record(evs[2], stream_handle)
-    moe.moe_combine(buf.y, buf.weights, buf.layout.dst_row, buf.out)
-    if ev is not None:
-        ev.record(evs[3], stream_handle)
+        ops = [("layout_dispatch", lambda b: b.layout.run_dispatch(
+            b.ids, b.tokens, b.packed, b.scales, fp8=fp8))]
+    ops.append(("combine", lambda b: moe.moe_combine(b.y, b.weights, b.layout.dst_row, b.out)))
+    return ops
+
+
+def run_step(moe, buf, dispatch, unfused=False):
+    for _, fn in step_ops(moe, dispatch, unfused):
+        fn(buf)
 
 
 def capture(torch, steps_fn, n_steps):
@@ -393,6 +401,33 @@ def time_oracle(w, dispatch, inp, y_bits, seconds: float, max_tokens=None):
             return T * n / el, T, n
 
 
+def graph_timer(torch, sets, n_sets, G, K):
+    """Returns time_ops(fn_step, n_steps) -> ms: captures fn over the rotating
+    sets into CUDA graphs of G steps (plus one of the remainder) and times
+    n_steps of them between CUDA events on the launching stream."""
+    def build(fn, n):
+        return capture(torch, lambda m, sh: [fn(sets[j % n_sets]) for j in range(m)], n)
+
+    def time_ops(fn, n_steps, warmup):
+        g = build(fn, G)
+        rem = n_steps % G
+        gr = build(fn, rem) if rem else None
+        for _ in range(max(1, warmup // G)):
+            g.replay()
+        start = torch.cuda.Event(enable_timing=True)
+        stop = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        start.record()
+        for _ in range(n_steps // G):
+            g.replay()
+        if gr is not None:
+            gr.replay()
+        stop.record()
+        torch.cuda.synchronize()
+        return start.elapsed_time(stop)
+    return time_ops
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -415,53 +450,36 @@ def run_ours(args):
     w = wl.get(args.workload or wl.HEADLINE)
     dispatch = args.dispatch or w.dispatch[0]
     inp = wl.make_inputs(w, seed=shard_seed(w.seed, rank))
+    ops = step_ops(moe, dispatch, args.unfused)
 
     # rotating buffer sets: total >= 3x L2, so every step starts cold in L2
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
     first = BufferSet(w, dispatch, inp, None, device)
-    run_step_nograph = lambda b: (b.layout.run(b.ids), moe.moe_dispatch(
-        b.tokens, b.layout.dst_row, b.packed, b.scales, fp8=(dispatch == "fp8")))
-    run_step_nograph(first)
+    ops[0][1](first)
+    if args.unfused:
+        ops[1][1](first)
     torch.cuda.synchronize()
     y_bits = expert_outputs(w, dispatch, inp, first)
     per_set = first.nbytes() + y_bits.nbytes
     n_sets = max(2, math.ceil(3 * l2 / per_set))
     sets = [BufferSet(w, dispatch, inp, y_bits, device) for _ in range(n_sets)]
     del first
-
-    ev = Driver()
-    G = max(n_sets, (min(args.graph_steps, max(args.steps, 1)) // n_sets) * n_sets)
-    K = args.steps
-
-    def make_graph(n_steps, with_events):
-        evs = [[ev.event() for _ in range(4)] for _ in range(n_steps)] if with_events else None
-
-        def body(n, sh):
-            for j in range(n):
-                run_step(moe, sets[j % n_sets], dispatch, ev if with_events else None,
-                         evs[j] if with_events else None, sh)
-        for j in range(min(n_steps, n_sets)):      # eager warm-up (attributes, caches)
-            run_step(moe, sets[j], dispatch)
-        torch.cuda.synchronize()
-        return capture(torch, body, n_steps), evs
-
-    gA, evA = make_graph(G, True)
-    rem = K % G
-    gB, evB = make_graph(rem, True) if rem else (None, None)
-
-    def replay(nsteps):
-        for _ in range(nsteps // G):
-            gA.replay()
-        if nsteps % G:
-            if nsteps % G == rem and gB is not None:
-                gB.replay()
-            else:
-                for j in range(nsteps % G):
-                    run_step(moe, sets[j % n_sets], dispatch)
-
-    replay(args.warmup)
+    for b in sets:                       # eager pass: attributes, parity data
+        run_step(moe, b, dispatch, args.unfused)
     torch.cuda.synchronize()
-    parity = check_parity(w, dispatch, inp, sets[0]) if rank == 0 else None
+
+    K = args.steps
+    G = max(n_sets, (min(args.graph_steps, max(K, 1)) // n_sets) * n_sets)
+    step = lambda b: run_step(moe, b, dispatch, args.unfused)
+    g = capture(torch, lambda m, sh: [step(sets[j % n_sets]) for j in range(m)], G)
+    rem = K % G
+    gr = capture(torch, lambda m, sh: [step(sets[j % n_sets]) for j in range(m)], rem) if rem else None
+    for _ in range(max(1, args.warmup // G)):
+        g.replay()
+    for j in range(args.warmup % G):
+        step(sets[j % n_sets])
+    torch.cuda.synchronize()
+    parity = check_parity(w, dispatch, inp, sets[-1]) if rank == 0 else None
 
     sampler = ClockSampler(local)
     sampler.start()
@@ -472,37 +490,36 @@ def run_ours(args):
     torch.cuda.synchronize()
     sampler.mark_start()
     start.record()
-    replay(K)
+    for _ in range(K // G):
+        g.replay()
+    if gr is not None:
+        gr.replay()
     stop.record()
     torch.cuda.synchronize()
     sampler.mark_stop()
     barrier(device)
     time.sleep(0.15)
     clocks = sampler.stop()
-    elapsed_ms = start.elapsed_time(stop)
-    elapsed_ms = max_over_ranks(elapsed_ms, device)
+    elapsed_ms = max_over_ranks(start.elapsed_time(stop), device)
 
-    # per-kernel durations from the last replay of each graph
-    per_kernel = {k: [] for k in KERNELS}
-    for evs, n in ((evA, min(G, K) if K >= G else 0), (evB, rem)):
-        if not evs:
-            continue
-        for j in range(n):
-            for i, k in enumerate(KERNELS):
-                per_kernel[k].append(ev.ms(evs[j][i], evs[j][i + 1]))
-    avg_us = {k: 1e3 * statistics.fmean(v) for k, v in per_kernel.items() if v}
+    # each call of the step alone: K launches over the same rotating sets
+    time_ops = graph_timer(torch, sets, n_sets, G, K)
     ab = algorithmic_bytes(w, dispatch)
     peak, peak_src = read_peaks()
-    kernels = {k: {"us": round(avg_us[k], 3),
-                   "gbs": round(ab[k] / (avg_us[k] * 1e-6) / 1e9, 1),
-                   "bytes": ab[k]} for k in avg_us}
-    dom = max(avg_us, key=lambda k: avg_us[k]) if avg_us else "combine"
-    achieved = kernels[dom]["gbs"] if dom in kernels else None
+    kernels = {}
+    for name, fn in ops:
+        ms = time_ops(fn, K, args.warmup)
+        us = 1e3 * ms / K
+        kernels[name] = {"us": round(us, 3), "gbs": round(ab[name] / (us * 1e-6) / 1e9, 1),
+                         "bytes": ab[name]}
+    dom = max(kernels, key=lambda k: kernels[k]["us"])
+    achieved = kernels[dom]["gbs"]
 
+    drv = Driver()
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(args, w, dispatch, inp, sets, n_sets, device, torch, moe, ev)
-    ev.close()
+        e2e = run_e2e(args, w, dispatch, inp, sets, n_sets, device, torch, moe, drv)
+    drv.close()
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline and world == 1:
@@ -521,16 +538,19 @@ def run_ours(args):
         "config": {"workload": w.name, "T": w.T, "H": w.H, "E": w.E, "R": w.R,
                    "K": w.K, "dispatch": dispatch, "combine": "bf16 in, f32 accumulate",
                    "experts": w.experts, "routing": w.routing,
+                   "calls": [n for n, _ in ops],
                    "l2": f"{n_sets} rotating buffer sets, {n_sets * per_set / 1e6:.0f} MB "
                          f"> 3x L2 ({l2 / 1e6:.0f} MB); every step cold in L2",
-                   "launch": f"CUDA graphs of {G} steps, event nodes around each kernel",
+                   "launch": f"CUDA graphs of {G} steps, programmatic dependent launch",
+                   "kernel_timing": "each call alone: K launches in CUDA graphs over the "
+                                    "same rotating sets, CUDA events around the replays",
                    "parallelism": f"replicas x{world}"},
         "kernels": kernels,
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
-                     "unit": "GB/s", "frac": round(achieved / peak, 4) if achieved else None,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "peak_source": peak_src,
                      "traffic": profiled_traffic(dom, w.name, dispatch)},
-        "e2e": e2e, "gpu_launches": launches_per_step(w) * K,
+        "e2e": e2e, "gpu_launches": launches_per_step(w, dispatch, args.unfused) * K,
         "clocks": clocks, "cpu_baseline": cpu, "parity": parity,
     }
     if rank == 0:
@@ -540,10 +560,13 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def launches_per_step(w) -> int:
+def launches_per_step(w, dispatch, unfused) -> int:
+    """Kernels this library launches per step (mirrors the C ABI's plans)."""
     import combine_moe_layout_05_gb300 as moe
-    fused = moe.moe_layout_workspace_bytes(w.T, w.K, w.E) == 0
-    return (1 if fused else 2) + 2
+    layout_kernels = 1 if moe.moe_layout_workspace_bytes(w.T, w.K, w.E) == 0 else 2
+    if unfused:
+        return layout_kernels + 2
+    return moe.moe_layout_dispatch_kernels(w.T, w.H, w.K, w.E, dispatch == "fp8") + 1
 
 
 def run_e2e(args, w, dispatch, inp, sets, n_sets, device, torch, moe, drv):
@@ -570,12 +593,11 @@ def run_e2e(args, w, dispatch, inp, sets, n_sets, device, torch, moe, drv):
             drv.h2d(b.tokens.data_ptr(), *h["tokens"], sh)
             drv.h2d(b.ids.data_ptr(), *h["ids"], sh)
             drv.h2d(b.weights.data_ptr(), *h["weights"], sh)
-            run_step(moe, b, dispatch)
+            run_step(moe, b, dispatch, args.unfused)
             drv.d2h(h["out"], b.out.data_ptr(), d2h, sh)
 
     K = args.steps
     G = max(n_sets, (min(args.graph_steps, max(K, 1)) // n_sets) * n_sets)
-    body(n_sets, torch.cuda.current_stream().cuda_stream)
     torch.cuda.synchronize()
     g = capture(torch, body, G)
     rem = K % G

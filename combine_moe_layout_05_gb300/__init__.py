@@ -9,12 +9,15 @@ dispatch and combine.
 from ._binding import (MOE_DEV_ERR_DUPLICATE, MOE_DEV_ERR_EXPERT_RANGE,
                        LayoutBuffers, MoeError, declared_functions,
                        library_path, load, moe_combine, moe_dispatch,
-                       moe_layout, moe_layout_workspace_bytes,
+                       moe_layout, moe_layout_dispatch,
+                       moe_layout_dispatch_kernels,
+                       moe_layout_workspace_bytes,
                        moe_status_string)
 
 __all__ = [
     "MOE_DEV_ERR_DUPLICATE", "MOE_DEV_ERR_EXPERT_RANGE", "LayoutBuffers",
     "MoeError", "declared_functions", "library_path", "load", "moe_combine",
-    "moe_dispatch", "moe_layout", "moe_layout_workspace_bytes",
+    "moe_dispatch", "moe_layout", "moe_layout_dispatch", "moe_layout_dispatch_kernels",
+    "moe_layout_workspace_bytes",
     "moe_status_string",
 ]

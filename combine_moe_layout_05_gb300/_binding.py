@@ -57,6 +57,11 @@ def load(path: str | None = None):
             lib.moe_dispatch.restype = ctypes.c_int
             lib.moe_combine.argtypes = [P, P, P, i32, i32, i32, P, P]
             lib.moe_combine.restype = ctypes.c_int
+            lib.moe_layout_dispatch.argtypes = [P, P, i32, i32, i32, i32, i32, i32,
+                                                P, P, P, P, P, P, P, P, P, sz, P]
+            lib.moe_layout_dispatch.restype = ctypes.c_int
+            lib.moe_layout_dispatch_kernels.argtypes = [i32, i32, i32, i32, i32]
+            lib.moe_layout_dispatch_kernels.restype = i32
             _lib = lib
     return _lib
 
@@ -102,6 +107,10 @@ def moe_status_string(status: int) -> str:
 
 def moe_layout_workspace_bytes(T: int, K: int, E: int) -> int:
     return int(load().moe_layout_workspace_bytes(T, K, E))
+
+
+def moe_layout_dispatch_kernels(T: int, H: int, K: int, E: int, fp8: bool) -> int:
+    return int(load().moe_layout_dispatch_kernels(T, H, K, E, int(bool(fp8))))
 
 
 def moe_layout(topk_ids, E: int, R: int, expert_counts, expert_offsets,
@@ -150,6 +159,43 @@ def moe_dispatch(tokens, dst_row, packed, scales=None, fp8: bool = False,
     _raise("moe_dispatch", st)
 
 
+def moe_layout_dispatch(topk_ids, tokens, E: int, R: int, expert_counts,
+                        expert_offsets, rank_offsets, src_token, dst_row, packed,
+                        scales=None, fp8: bool = False, dev_error=None,
+                        workspace=None, stream=None) -> None:
+    """moe_layout then moe_dispatch in one call (one kernel for small batches)."""
+    T, K = topk_ids.shape
+    H = tokens.shape[1]
+    if tokens.shape[0] != T:
+        raise ValueError("moe_layout_dispatch: tokens and topk_ids disagree on T")
+    _check("topk_ids", topk_ids, torch.int32)
+    _check("tokens", tokens, torch.bfloat16)
+    for n, t in (("expert_counts", expert_counts), ("expert_offsets", expert_offsets),
+                 ("rank_offsets", rank_offsets), ("src_token", src_token),
+                 ("dst_row", dst_row)):
+        _check(n, t, torch.int32)
+    if expert_counts.numel() < E or expert_offsets.numel() < E + 1 or rank_offsets.numel() < R + 1:
+        raise ValueError("moe_layout_dispatch: output arrays too small")
+    if src_token.numel() < T * K or dst_row.numel() < T * K or packed.numel() < T * K * H:
+        raise ValueError("moe_layout_dispatch: src_token/dst_row/packed too small")
+    if fp8:
+        _check("packed", packed, torch.float8_e4m3fn)
+        _check("scales", scales, torch.float32)
+        if scales is None or scales.numel() < T * K * (H // 128):
+            raise ValueError("moe_layout_dispatch: scales missing or too small")
+    else:
+        _check("packed", packed, torch.bfloat16)
+    if dev_error is not None:
+        _check("dev_error", dev_error, torch.int32)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = load().moe_layout_dispatch(
+        _ptr(topk_ids), _ptr(tokens), T, H, K, E, R, int(bool(fp8)), _ptr(expert_counts),
+        _ptr(expert_offsets), _ptr(rank_offsets), _ptr(src_token), _ptr(dst_row),
+        _ptr(dev_error), _ptr(packed), _ptr(scales) if fp8 else None,
+        _ptr(workspace), ws_bytes, _stream(stream))
+    _raise("moe_layout_dispatch", st)
+
+
 def moe_combine(expert_out, topk_weights, dst_row, out, stream=None) -> None:
     """Routing-weighted fp32 sum of each token's K expert rows, rounded to bf16."""
     T, K = topk_weights.shape
@@ -184,4 +230,13 @@ class LayoutBuffers:
         moe_layout(topk_ids, self.E, self.R, self.expert_counts,
                    self.expert_offsets, self.rank_offsets, self.src_token,
                    self.dst_row, self.dev_error, self.workspace, stream)
+        return self
+
+    def run_dispatch(self, topk_ids, tokens, packed, scales=None, fp8=False,
+                     stream=None) -> "LayoutBuffers":
+        """Layout and dispatch together (moe_layout_dispatch)."""
+        moe_layout_dispatch(topk_ids, tokens, self.E, self.R, self.expert_counts,
+                            self.expert_offsets, self.rank_offsets, self.src_token,
+                            self.dst_row, packed, scales, fp8, self.dev_error,
+                            self.workspace, stream)
         return self

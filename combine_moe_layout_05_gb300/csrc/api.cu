@@ -107,4 +107,49 @@ moe_status_t moe_combine(const void *expert_out, const float *topk_weights,
                                            H, K, out, stream));
 }
 
+moe_status_t moe_layout_dispatch(const int32_t *topk_ids, const void *tokens,
+                                 int32_t T, int32_t H, int32_t K, int32_t E,
+                                 int32_t R, int32_t fp8, int32_t *expert_counts,
+                                 int32_t *expert_offsets, int32_t *rank_offsets,
+                                 int32_t *src_token, int32_t *dst_row,
+                                 uint32_t *dev_error, void *packed, float *scales,
+                                 void *workspace, size_t workspace_bytes,
+                                 cudaStream_t stream)
+{
+    if (!layout_sizes_ok(T, K, E) || R < 1 || E % R != 0) return MOE_ERR_INVALID_ARG;
+    moe_status_t s = rows_ok(T, H, K);
+    if (s != MOE_OK) return s;
+    if (fp8 != 0 && fp8 != 1) return MOE_ERR_INVALID_ARG;
+    if (fp8 && H % 128 != 0) return MOE_ERR_INVALID_ARG;
+    if (!expert_counts || !expert_offsets || !rank_offsets) return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (!topk_ids || !src_token || !dst_row || !tokens || !packed ||
+                  (fp8 && !scales)))
+        return MOE_ERR_INVALID_ARG;
+    const void *p4[] = {topk_ids, expert_counts, expert_offsets, rank_offsets,
+                        src_token, dst_row, dev_error, fp8 ? scales : nullptr};
+    for (const void *p : p4)
+        if (!aligned(p, 4)) return MOE_ERR_ALIGNMENT;
+    if (!aligned(tokens, 16) || !aligned(packed, 16)) return MOE_ERR_ALIGNMENT;
+    if (!moe::layout_dispatch_fused(T, H, K, fp8)) {
+        const size_t need = moe::layout_workspace_bytes(moe::plan_layout(T, K, E), E);
+        if (need > 0) {
+            if (!workspace || workspace_bytes < need) return MOE_ERR_WORKSPACE;
+            if (!aligned(workspace, 16)) return MOE_ERR_ALIGNMENT;
+        }
+    }
+    return cuda_status(moe::launch_layout_dispatch(
+        topk_ids, tokens, T, H, K, E, R, fp8, expert_counts, expert_offsets,
+        rank_offsets, src_token, dst_row, dev_error, packed, scales, workspace, stream));
+}
+
+int32_t moe_layout_dispatch_kernels(int32_t T, int32_t H, int32_t K, int32_t E,
+                                    int32_t fp8)
+{
+    if (!layout_sizes_ok(T, K, E) || rows_ok(T, H, K) != MOE_OK) return 0;
+    if ((fp8 != 0 && fp8 != 1) || (fp8 && H % 128 != 0)) return 0;
+    if (moe::layout_dispatch_fused(T, H, K, fp8)) return 1;
+    const int layout = moe::plan_layout(T, K, E).fused ? 1 : 2;
+    return T > 0 ? layout + 1 : layout;
+}
+
 }  // extern "C"

@@ -42,6 +42,8 @@ combine_kernel(const uint4 *__restrict__ y, const float *__restrict__ weights,
                const int32_t *__restrict__ dst_row, int K, int vpr, int rows,
                uint4 *__restrict__ out)
 {
+    pdl_wait();
+    pdl_trigger();
     const int t = blockIdx.x;
     const int v = blockIdx.y * blockDim.x + threadIdx.x;
     if (v >= vpr) return;
@@ -84,11 +86,9 @@ cudaError_t run_combine(const void *y, const float *w, const int32_t *dst_row,
 {
     const int vpr = H / 8;
     const int threads = pick_row_block(vpr);
-    const dim3 grid(T, ceil_div(vpr, threads));
-    combine_kernel<KT><<<grid, threads, 0, s>>>(
-        static_cast<const uint4 *>(y), w, dst_row, K, vpr, T * K,
-        static_cast<uint4 *>(out));
-    return cudaGetLastError();
+    return launch_pdl(combine_kernel<KT>, dim3(T, ceil_div(vpr, threads)),
+                      dim3(threads), 0, s, static_cast<const uint4 *>(y), w,
+                      dst_row, K, vpr, T * K, static_cast<uint4 *>(out));
 }
 
 }  // namespace

@@ -36,6 +36,18 @@ cudaError_t launch_combine(const void *expert_out, const float *topk_weights,
                            const int32_t *dst_row, int T, int H, int K,
                            void *out, cudaStream_t stream);
 
+// Layout and dispatch together: one fused kernel when
+// layout_dispatch_fused() says the batch is small enough, else the layout
+// kernels followed by the dispatch kernel.
+bool layout_dispatch_fused(int T, int H, int K, int fp8);
+cudaError_t launch_layout_dispatch(const int32_t *topk_ids, const void *tokens,
+                                   int T, int H, int K, int E, int R, int fp8,
+                                   int32_t *expert_counts, int32_t *expert_offsets,
+                                   int32_t *rank_offsets, int32_t *src_token,
+                                   int32_t *dst_row, uint32_t *dev_error,
+                                   void *packed, float *scales, void *workspace,
+                                   cudaStream_t stream);
+
 // Threads per block for `units` work items per row: the largest multiple of
 // 32 up to 256 that divides `units`, else 128 (last block of a row partial).
 int pick_row_block(int units);

@@ -130,6 +130,8 @@ layout_count_kernel(const int32_t *__restrict__ ids, int T, int K, int E,
     for (int e = tid; e < E; e += kThreads) hist[e] = 0;
     if (tid == 0) s_err = 0;
     __syncthreads();
+    pdl_wait();
+    pdl_trigger();
 
     int lo, hi;
     warp_segment(n, w, lo, hi);
@@ -170,6 +172,8 @@ layout_rank_kernel(const int32_t *__restrict__ ids, int T, int K, int E, int R,
     for (int i = tid; i < kWarps * E; i += kThreads) hist[i] = 0;
     if (tid == 0) s_err = 0;
     __syncthreads();
+    pdl_wait();
+    pdl_trigger();
 
     // 1. per-warp counts of this block's entries
     int lo, hi;
@@ -324,25 +328,26 @@ cudaError_t launch_layout(const int32_t *topk_ids, int T, int K, int E, int R,
         const size_t smem = rank_smem_bytes(E, true);
         cudaError_t e = allow_smem((const void *)layout_rank_kernel<true>, smem);
         if (e != cudaSuccess) return e;
-        layout_rank_kernel<true><<<1, kThreads, smem, stream>>>(
-            topk_ids, T, K, E, R, T, 1, nullptr, nullptr, expert_counts,
-            expert_offsets, rank_offsets, src_token, dst_row, dev_error);
-        return cudaGetLastError();
+        return launch_pdl(layout_rank_kernel<true>, dim3(1), dim3(kThreads), smem,
+                          stream, topk_ids, T, K, E, R, T, 1,
+                          (const int32_t *)nullptr, (const uint32_t *)nullptr,
+                          expert_counts, expert_offsets, rank_offsets, src_token,
+                          dst_row, dev_error);
     }
     int32_t *ws_hist = static_cast<int32_t *>(workspace);
     uint32_t *ws_err = reinterpret_cast<uint32_t *>(ws_hist + (size_t)plan.chunks * E);
-    layout_count_kernel<<<plan.chunks, kThreads, sizeof(int32_t) * E, stream>>>(
-        topk_ids, T, K, E, plan.tokens_per_chunk, ws_hist, ws_err);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(layout_count_kernel, dim3(plan.chunks), dim3(kThreads),
+                               sizeof(int32_t) * E, stream, topk_ids, T, K, E,
+                               plan.tokens_per_chunk, ws_hist, ws_err);
     if (e != cudaSuccess) return e;
     const size_t smem = rank_smem_bytes(E, false);
     e = allow_smem((const void *)layout_rank_kernel<false>, smem);
     if (e != cudaSuccess) return e;
-    layout_rank_kernel<false><<<plan.chunks, kThreads, smem, stream>>>(
-        topk_ids, T, K, E, R, plan.tokens_per_chunk, plan.chunks, ws_hist,
-        ws_err, expert_counts, expert_offsets, rank_offsets, src_token,
-        dst_row, dev_error);
-    return cudaGetLastError();
+    return launch_pdl(layout_rank_kernel<false>, dim3(plan.chunks), dim3(kThreads),
+                      smem, stream, topk_ids, T, K, E, R, plan.tokens_per_chunk,
+                      plan.chunks, (const int32_t *)ws_hist, (const uint32_t *)ws_err,
+                      expert_counts, expert_offsets, rank_offsets, src_token,
+                      dst_row, dev_error);
 }
 
 }  // namespace moe

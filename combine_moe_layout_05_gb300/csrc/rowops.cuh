@@ -1,0 +1,102 @@
+// rowops.cuh -- the per-thread pieces of dispatch shared by the plain
+// dispatch kernels and the fused layout+dispatch kernel: writing one 16-byte
+// piece of a token row to all of its slots, and quantising 16 values of a
+// 1x128 block to e4m3 with the block's scale.
+#pragma once
+
+#include "common.cuh"
+#include "moe_layout.h"
+
+namespace moe {
+
+// Writes `x` (16 bytes at byte offset `off` of a packed row) to each slot in
+// slots[0 .. k_count); slots outside [0, rows) are skipped.  `slots` may
+// point to global or shared memory.  KT > 0 is a compile-time k_count.
+template <int KT>
+__device__ __forceinline__ void store_to_slots(const int32_t *slots, int k_count,
+                                               int rows, uint8_t *packed,
+                                               size_t row_bytes, size_t off,
+                                               const uint4 &x)
+{
+#pragma unroll
+    for (int k = 0; k < (KT > 0 ? KT : MOE_MAX_TOPK); ++k) {
+        if (KT == 0 && k >= k_count) break;
+        const int r = slots[k];
+        if ((unsigned)r < (unsigned)rows) st_v4(packed + (size_t)r * row_bytes + off, x);
+    }
+}
+
+// Block-scaled e4m3 of the 16 bf16 values in (a, b).  The 8 consecutive
+// lanes holding one 128-value block must all call this together (xor
+// shuffles over lane groups of 8; every lane of the warp participates).
+// amax is exact in fp32, scale = amax / 448 and every value is divided by
+// the scale with IEEE round-to-nearest division before the saturating
+// round-to-nearest-even conversion; an all-zero block keeps only the signs.
+struct Fp8Piece {
+    uint4 codes;
+    float scale;
+};
+
+__device__ __forceinline__ Fp8Piece quantize16(const uint4 &a, const uint4 &b)
+{
+    float x[16];
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        x[2 * i] = bf16_lo(w[i]);
+        x[2 * i + 1] = bf16_hi(w[i]);
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
+    amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 2));
+    amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 4));
+
+    Fp8Piece p;
+    p.scale = __fdiv_rn(amax, 448.0f);
+    uint32_t q[4];
+    if (amax == 0.0f) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            uint32_t s = 0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                s |= (__float_as_uint(x[4 * i + j]) >> 31) << (8 * j + 7);
+            q[i] = s;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t lo = cvt_e4m3x2_satfinite(__fdiv_rn(x[4 * i], p.scale),
+                                                     __fdiv_rn(x[4 * i + 1], p.scale));
+            const uint32_t hi = cvt_e4m3x2_satfinite(__fdiv_rn(x[4 * i + 2], p.scale),
+                                                     __fdiv_rn(x[4 * i + 3], p.scale));
+            q[i] = lo | (hi << 16);
+        }
+    }
+    p.codes = make_uint4(q[0], q[1], q[2], q[3]);
+    return p;
+}
+
+// Writes a quantised piece (group g of 16 values) and, from the block's
+// first lane, its scale, to each slot.
+template <int KT>
+__device__ __forceinline__ void store_fp8_to_slots(const int32_t *slots, int k_count,
+                                                   int rows, uint8_t *packed,
+                                                   float *scales, int H, int g,
+                                                   const Fp8Piece &p)
+{
+    const int nb = H >> 7;
+    const bool leader = (g & 7) == 0;
+#pragma unroll
+    for (int k = 0; k < (KT > 0 ? KT : MOE_MAX_TOPK); ++k) {
+        if (KT == 0 && k >= k_count) break;
+        const int r = slots[k];
+        if ((unsigned)r >= (unsigned)rows) continue;
+        st_v4(packed + (size_t)r * H + 16 * (size_t)g, p.codes);
+        if (leader) scales[(size_t)r * nb + (g >> 3)] = p.scale;
+    }
+}
+
+}  // namespace moe

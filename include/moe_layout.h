@@ -111,12 +111,12 @@ MOE_API size_t moe_layout_workspace_bytes(int32_t T, int32_t K, int32_t E);
  * T == 0 writes zero counts and offsets.
  */
 MOE_API moe_status_t moe_layout(const int32_t *topk_ids, int32_t T, int32_t K,
-                        int32_t E, int32_t R,
-                        int32_t *expert_counts, int32_t *expert_offsets,
-                        int32_t *rank_offsets, int32_t *src_token,
-                        int32_t *dst_row, uint32_t *dev_error,
-                        void *workspace, size_t workspace_bytes,
-                        cudaStream_t stream);
+                                int32_t E, int32_t R,
+                                int32_t *expert_counts, int32_t *expert_offsets,
+                                int32_t *rank_offsets, int32_t *src_token,
+                                int32_t *dst_row, uint32_t *dev_error,
+                                void *workspace, size_t workspace_bytes,
+                                cudaStream_t stream);
 
 /*
  * moe_dispatch -- pack every token row into each of its K slots.
@@ -144,8 +144,8 @@ MOE_API moe_status_t moe_layout(const int32_t *topk_ids, int32_t T, int32_t K,
  * H >= 8 with H % 8 == 0 (H % 128 == 0 when fp8 == 1).  T == 0 is a no-op.
  */
 MOE_API moe_status_t moe_dispatch(const void *tokens, int32_t T, int32_t H, int32_t K,
-                          const int32_t *dst_row, int32_t fp8, void *packed,
-                          float *scales, cudaStream_t stream);
+                                  const int32_t *dst_row, int32_t fp8, void *packed,
+                                  float *scales, cudaStream_t stream);
 
 /*
  * moe_combine -- routing-weighted sum of each token's K expert outputs.
@@ -170,6 +170,36 @@ MOE_API moe_status_t moe_dispatch(const void *tokens, int32_t T, int32_t H, int3
 MOE_API moe_status_t moe_combine(const void *expert_out, const float *topk_weights,
                          const int32_t *dst_row, int32_t T, int32_t H,
                          int32_t K, void *out, cudaStream_t stream);
+
+/*
+ * moe_layout_dispatch -- moe_layout followed by moe_dispatch, as one call.
+ *
+ * The page's dispatch-send kernel counts, scans and packs in one pass
+ * ("Dispatch and Combine").  Every output is bit-identical to calling
+ * moe_layout and then moe_dispatch with the same arguments.  For small
+ * batches (decode shapes: T*K <= 8192 and a bounded amount of redundant
+ * histogram work) it runs as a single kernel launch; larger batches run the
+ * layout kernels and then the dispatch kernel.
+ *
+ * Arguments are those of moe_layout and moe_dispatch together, with the same
+ * layouts, alignment and limits.  workspace: as for moe_layout (a buffer of
+ * moe_layout_workspace_bytes(T,K,E) bytes always suffices; the single-kernel
+ * path uses none).
+ */
+MOE_API moe_status_t moe_layout_dispatch(const int32_t *topk_ids, const void *tokens,
+                                         int32_t T, int32_t H, int32_t K, int32_t E,
+                                         int32_t R, int32_t fp8, int32_t *expert_counts,
+                                         int32_t *expert_offsets, int32_t *rank_offsets,
+                                         int32_t *src_token, int32_t *dst_row,
+                                         uint32_t *dev_error, void *packed, float *scales,
+                                         void *workspace, size_t workspace_bytes,
+                                         cudaStream_t stream);
+
+/* Number of kernel launches moe_layout_dispatch makes for these sizes: 1
+ * when it runs as a single kernel, 2 or 3 otherwise (moe_layout's one or two
+ * kernels, then moe_dispatch's).  0 for invalid sizes. */
+MOE_API int32_t moe_layout_dispatch_kernels(int32_t T, int32_t H, int32_t K,
+                                            int32_t E, int32_t fp8);
 
 #ifdef __cplusplus
 }

@@ -92,3 +92,30 @@ def test_combine_host_checks(lib):
     assert c(P(FAKE), P(FAKE + 2), P(FAKE), 4, 128, 2, P(FAKE), None) == 2
     assert c(P(FAKE), P(FAKE), None, 4, 128, 2, P(FAKE), None) == 1
     assert c(None, None, None, 0, 128, 2, None, None) == 0              # T == 0: no-op
+
+
+def test_layout_dispatch_plan_query(lib):
+    # decode shapes run as one kernel, prefill shapes as layout + dispatch
+    assert moe.moe_layout_dispatch_kernels(128, 7168, 8, 256, False) == 1
+    assert moe.moe_layout_dispatch_kernels(256, 7168, 8, 256, True) == 1
+    assert moe.moe_layout_dispatch_kernels(4096, 7168, 8, 384, False) == 3
+    assert moe.moe_layout_dispatch_kernels(1000, 4096, 8, 128, False) == 2
+    assert moe.moe_layout_dispatch_kernels(0, 128, 4, 16, False) == 1
+    assert moe.moe_layout_dispatch_kernels(128, 100, 8, 256, False) == 0    # H % 8
+    assert moe.moe_layout_dispatch_kernels(128, 136, 8, 256, True) == 0     # H % 128
+
+
+def test_layout_dispatch_host_checks(lib):
+    f = lib.moe_layout_dispatch
+    args = lambda **kw: [P(kw.get("ids", FAKE)), P(kw.get("tok", FAKE)), kw.get("T", 4),
+                         kw.get("H", 128), kw.get("K", 2), kw.get("E", 8), kw.get("R", 2),
+                         kw.get("fp8", 0), P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(FAKE),
+                         None, P(kw.get("packed", FAKE)), P(kw.get("scales", FAKE)),
+                         P(kw.get("ws")) if kw.get("ws") else None, kw.get("wsb", 0), None]
+    assert f(*args(E=8, R=3)) == 1
+    assert f(*args(H=100)) == 1
+    assert f(*args(H=136, fp8=1)) == 1
+    assert f(*args(tok=FAKE + 8)) == 2
+    assert f(*args(packed=FAKE + 4)) == 2
+    assert f(*args(fp8=1, scales=FAKE + 2)) == 2
+    assert f(*args(T=4096, H=7168, K=8, E=384, R=48)) == 4       # needs workspace

@@ -214,7 +214,8 @@ def test_combine_fma_and_order_sensitive(oracle):
     w0 = np.float32(1 + 2.0 ** -23)
     y0 = np.float32(1 - 2.0 ** -8)
     rows = np.array([[y0] * 8, [-y0] * 8, [2.0 ** 30] * 8, [1.0] * 8,
-                     [-(2.0 ** 30)] * 8, [-0.0] * 8, [-0.0] * 8], np.float32)
+                     [-(2.0 ** 30)] * 8, [-0.0] * 8, [-0.0] * 8, [5.0] * 8,
+                     [7.0] * 8], np.float32)
     y = wl.to_bf16_bits(rows)
     wts = np.array([[w0, w0, 1], [1, 1, 1], [1, 1, 0.5]], np.float32)
     dst = np.array([[0, 1, 5], [2, 4, 3], [5, 6, 6]], np.int32)
@@ -273,3 +274,87 @@ def test_end_to_end_fp8(oracle, name):
         o = wl.bf16_bits_to_f32(bf16_host(out)).astype(np.float64).reshape(w.T, -1, 128)
         amax = np.abs(x).max(axis=2, keepdims=True)
         assert np.all(np.abs(o - x) <= amax / 28 * 1.01 + np.abs(x) * 2.0 ** -7)
+
+
+# ------------------------------------------- layout + dispatch in one call --
+
+FUSED_SHAPES = [  # T, H, K, E, R, fp8: single-kernel sizes, then fallbacks
+    (1, 8, 1, 1, 1, 0), (3, 24, 3, 7, 7, 0), (128, 7168, 8, 256, 32, 0),
+    (256, 7168, 8, 256, 32, 1), (128, 7168, 8, 256, 32, 1), (100, 1032, 6, 64, 8, 0),
+    (64, 256, 2, 8, 2, 1), (37, 4096, 32, 1024, 16, 0), (250, 384, 9, 1024, 4, 1),
+    (1024, 7168, 8, 256, 32, 0), (4096, 7168, 8, 384, 48, 1), (0, 128, 4, 16, 4, 0),
+]
+
+
+@pytest.mark.parametrize("T,H,K,E,R,fp8", FUSED_SHAPES)
+def test_layout_dispatch_matches_oracle(oracle, T, H, K, E, R, fp8):
+    rng = np.random.default_rng(T * 7 + H + K)
+    x = wl.to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32)
+                        * np.exp2(rng.integers(-8, 8, (T, 1))).astype(np.float32))
+    ids = wl.routing_zipf(T, E, K, 1.2, rng) if T else np.zeros((0, K), np.int32)
+    ref = oracle.layout(ids, E, R)
+    buf = moe.LayoutBuffers(T, K, E, R)
+    for t in (buf.expert_counts, buf.expert_offsets, buf.rank_offsets, buf.src_token,
+              buf.dst_row, buf.dev_error):
+        t.fill_(-7)
+    if fp8:
+        packed = torch.empty((T * K, H), dtype=torch.float8_e4m3fn, device="cuda")
+        packed.view(torch.uint8).fill_(0x7F)
+        scales = torch.full((T * K, H // 128), float("nan"), device="cuda")
+    else:
+        packed = torch.empty((T * K, H), dtype=torch.bfloat16, device="cuda")
+        packed.view(torch.int16).fill_(-1)
+        scales = None
+    buf.run_dispatch(i32_dev(ids), bf16_dev(x), packed, scales, fp8=bool(fp8))
+    torch.cuda.synchronize()
+    assert_layout_equal(buf, ref, T, K, E, R)
+    if T == 0:
+        return
+    if fp8:
+        ec, es = oracle.dispatch_fp8(x, ref.dst_row)
+        assert np.array_equal(packed.view(torch.uint8).cpu().numpy(), ec)
+        assert np.array_equal(scales.cpu().numpy().view(np.uint32), es.view(np.uint32))
+    else:
+        assert np.array_equal(bf16_host(packed), oracle.dispatch_bf16(x, ref.dst_row))
+
+
+@pytest.mark.parametrize("name", ALL)
+def test_layout_dispatch_full_size(oracle, name):
+    """The call the benchmark makes, at each workload's full size."""
+    w, inp, ref = _setup(oracle, name)
+    for fp8 in (False, True):
+        buf = moe.LayoutBuffers(w.T, w.K, w.E, w.R)
+        if fp8:
+            packed = torch.empty((w.T * w.K, w.H), dtype=torch.float8_e4m3fn, device="cuda")
+            scales = torch.empty((w.T * w.K, w.H // 128), device="cuda")
+        else:
+            packed = torch.empty((w.T * w.K, w.H), dtype=torch.bfloat16, device="cuda")
+            scales = None
+        buf.run_dispatch(i32_dev(inp.topk_ids), bf16_dev(inp.tokens), packed, scales, fp8=fp8)
+        torch.cuda.synchronize()
+        assert_layout_equal(buf, ref, w.T, w.K, w.E, w.R)
+        if fp8:
+            ec, es = oracle.dispatch_fp8(inp.tokens, ref.dst_row)
+            assert np.array_equal(packed.view(torch.uint8).cpu().numpy(), ec)
+            assert np.array_equal(scales.cpu().numpy().view(np.uint32), es.view(np.uint32))
+        else:
+            assert np.array_equal(bf16_host(packed), oracle.dispatch_bf16(inp.tokens, ref.dst_row))
+
+
+def test_layout_dispatch_bad_ids(oracle):
+    """Errors and -1 slots from the single-kernel path match the oracle's."""
+    rng = np.random.default_rng(1)
+    T, H, K, E, R = 50, 256, 4, 16, 4
+    ids = wl.routing_uniform(T, E, K, rng)
+    ids[0, 0] = E + 3
+    ids[9, 3] = ids[9, 1]
+    x = wl.to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32))
+    ref = oracle.layout(ids, E, R)
+    buf = moe.LayoutBuffers(T, K, E, R)
+    packed = torch.zeros((T * K, H), dtype=torch.bfloat16, device="cuda")
+    buf.run_dispatch(i32_dev(ids), bf16_dev(x), packed)
+    torch.cuda.synchronize()
+    assert_layout_equal(buf, ref, T, K, E, R)
+    exp = oracle.dispatch_bf16(x, ref.dst_row)
+    n = int(ref.expert_offsets[E])
+    assert np.array_equal(bf16_host(packed)[:n], exp[:n])
