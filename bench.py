@@ -563,7 +563,7 @@ def run_ours(args):
 def launches_per_step(w, dispatch, unfused) -> int:
     """Kernels this library launches per step (mirrors the C ABI's plans)."""
     import combine_moe_layout_05_gb300 as moe
-    layout_kernels = 1 if moe.moe_layout_workspace_bytes(w.T, w.K, w.E) == 0 else 2
+    layout_kernels = 1 if moe.moe_layout_workspace_bytes(w.T, w.K, w.E) == 0 else 3
     if unfused:
         return layout_kernels + 2
     return moe.moe_layout_dispatch_kernels(w.T, w.H, w.K, w.E, dispatch == "fp8") + 1

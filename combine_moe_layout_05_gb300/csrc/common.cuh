@@ -51,6 +51,31 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2_satfinite(float lo, float hi)
 }
 
 __host__ __device__ constexpr int ceil_div(int a, int b) { return (a + b - 1) / b; }
+__host__ __device__ constexpr int align4(int n) { return (n + 3) & ~3; }
+
+// Copies n int32 values from global to shared memory with asynchronous
+// copies issued by all threads of the block (every request is in flight at
+// once, so the block pays one memory latency, not one per loop trip).  The
+// caller must call cp_async_wait_all() and then __syncthreads().
+__device__ __forceinline__ void stage_i32(int32_t *dst, const int32_t *src, int n)
+{
+    const unsigned base = (unsigned)__cvta_generic_to_shared(dst);
+    const bool vec = ((reinterpret_cast<uintptr_t>(src) | base) & 15) == 0;
+    int done = 0;
+    if (vec) {
+        const int n4 = n >> 2;
+        for (int i = threadIdx.x; i < n4; i += blockDim.x)
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
+                         :: "r"(base + 16u * i), "l"(src + 4 * i) : "memory");
+        done = n4 << 2;
+    }
+    for (int i = done + threadIdx.x; i < n; i += blockDim.x)
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 4;"
+                     :: "r"(base + 4u * i), "l"(src + i) : "memory");
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // Programmatic dependent launch.  Every kernel here is launched with
 // programmatic stream serialisation, so it may start while the previous

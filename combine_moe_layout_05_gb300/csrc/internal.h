@@ -10,7 +10,7 @@ namespace moe {
 
 // How the layout of T*K entries is split over thread blocks.
 struct LayoutPlan {
-    bool fused;            // one block does everything (no workspace)
+    bool single_launch;    // one kernel, no workspace
     int tokens_per_chunk;  // tokens per block in the multi-block path
     int chunks;            // number of blocks in the multi-block path
 };

@@ -9,22 +9,26 @@
 //
 // Order inside an expert's range: token ascending, then k (a stable counting
 // sort of the flat topk_ids array).  Shared-memory atomics alone give the
-// right counts but an arbitrary order, so every warp owns a contiguous
-// segment of the entries and keeps a private per-expert counter row:
-//   1. each warp counts its segment (warp match + one add per distinct id);
-//   2. per expert, the warp rows are scanned in warp order, the expert
-//      totals are scanned across experts (warp-shuffle block scan), and each
-//      warp's row becomes the first free slot of each expert for that warp;
-//   3. each warp walks its segment again 32 entries at a time; an entry's
-//      slot is its warp's counter plus the number of lower lanes holding the
-//      same id, and the highest such lane advances the counter.
-// Small batches (up to kFusedMaxEntries entries) run as one block.  Larger
-// ones split the tokens into chunks: a counting kernel writes each chunk's
-// histogram to the workspace, then the ranking kernel's block for chunk c
-// adds the histograms of chunks before c to its per-expert bases.  No block
-// ever waits for another block.
+// right counts but an arbitrary order, so the entries are split into
+// contiguous chunks (one per block) and, inside a block, contiguous
+// segments (one per warp); a slot is
+//     offsets[e] + (entries of e in earlier chunks)
+//                + (entries of e in earlier segments of this chunk)
+//                + (entries of e earlier in this warp's segment),
+// the last term counted 32 entries at a time with a warp match.
+//
+// Every block first copies its ids into shared memory with asynchronous
+// copies, so it waits for memory once instead of once per loop trip.
+//
+// Small batches (T*K <= kSelfMaxEntries) take one launch: each block stages
+// all T*K ids and counts the totals and the entries before its chunk itself.
+// Larger batches take three launches and a workspace, with no block ever
+// waiting for another: a counting kernel writes each chunk's histogram, a
+// one-block kernel turns the histograms into per-chunk prefixes and the
+// expert offsets, and the ranking kernel assigns the slots.
 #include "common.cuh"
 #include "internal.h"
+#include "layout_common.cuh"
 #include "moe_layout.h"
 
 #include <mutex>
@@ -32,243 +36,219 @@
 namespace moe {
 namespace {
 
-constexpr int kThreads = 1024;
+constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kFusedMaxEntries = 8192;
-constexpr int kChunkEntries = 4096;
-constexpr int kMaxChunks = 128;
+constexpr int kSelfMaxEntries = 4096;
+constexpr int kSelfChunk = 512;
+constexpr int kChunk = 1024;
+constexpr int kMaxChunks = 16384;
+constexpr int kScanThreads = 1024;
 
-// The warp's share [lo, hi) of a block's n entries: contiguous, 32-aligned.
-__device__ __forceinline__ void warp_segment(int n, int w, int &lo, int &hi)
-{
-    const int seg = ((n + kWarps - 1) / kWarps + 31) & ~31;
-    lo = min(n, w * seg);
-    hi = min(n, lo + seg);
-}
-
-// Adds the ids in ids[lo, hi) to hist[id].  With kAtomic the row is shared
-// by all warps of the block; without, it belongs to this warp alone.
-template <bool kAtomic>
-__device__ __forceinline__ uint32_t warp_count(const int32_t *__restrict__ ids,
-                                               int lo, int hi, int E,
-                                               int lane, int32_t *hist)
-{
-    uint32_t err = 0;
-    for (int b = lo; b < hi; b += 32) {
-        const int i = b + lane;
-        const bool valid = i < hi;
-        const int id = valid ? __ldg(ids + i) : 0;
-        const bool ok = valid && (unsigned)id < (unsigned)E;
-        if (valid && !ok) err |= MOE_DEV_ERR_EXPERT_RANGE;
-        const unsigned m = __match_any_sync(kFullMask, ok ? id : -1 - lane);
-        if (ok && lane == 31 - __clz(m)) {
-            if (kAtomic) atomicAdd(hist + id, __popc(m));
-            else hist[id] += __popc(m);
-        }
-    }
-    return err;
-}
-
-// A token that lists one valid expert twice.
-__device__ uint32_t check_duplicates(const int32_t *__restrict__ ids,
-                                     int ntok, int K, int E)
-{
-    uint32_t err = 0;
-    for (int t = threadIdx.x; t < ntok; t += blockDim.x) {
-        const int32_t *row = ids + (size_t)t * K;
-        for (int a = 0; a < K; ++a) {
-            const int ea = __ldg(row + a);
-            if ((unsigned)ea >= (unsigned)E) continue;
-            for (int b = a + 1; b < K; ++b)
-                if (__ldg(row + b) == ea) err |= MOE_DEV_ERR_DUPLICATE;
-        }
-    }
-    return err;
-}
-
-// Exclusive prefix sum of one value per thread over the whole block (all
-// kThreads threads must call).  `total` receives the block sum.
-__device__ __forceinline__ int block_exclusive_scan(int v, int32_t *warp_sums,
-                                                    int &total)
-{
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    int x = v;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-        const int y = __shfl_up_sync(kFullMask, x, d);
-        if (lane >= d) x += y;
-    }
-    if (lane == 31) warp_sums[w] = x;
-    __syncthreads();
-    if (w == 0) {
-        int s = warp_sums[lane];
-#pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-            const int y = __shfl_up_sync(kFullMask, s, d);
-            if (lane >= d) s += y;
-        }
-        warp_sums[lane] = s;
-    }
-    __syncthreads();
-    total = warp_sums[kWarps - 1];
-    return (w ? warp_sums[w - 1] : 0) + x - v;
-}
-
-// Multi-block path, pass 1: histogram of chunk blockIdx.x into the workspace.
+// Multi-launch path, kernel 1: histogram and error bits of chunk c.
+// ws_cnt is expert-major: ws_cnt[e * chunks + c].
 __global__ void __launch_bounds__(kThreads)
-layout_count_kernel(const int32_t *__restrict__ ids, int T, int K, int E,
-                    int tpc, int32_t *__restrict__ ws_hist,
+layout_count_kernel(const int32_t *__restrict__ ids, int T, int K, int E, int tpc,
+                    int chunks, int32_t *__restrict__ ws_cnt,
                     uint32_t *__restrict__ ws_err)
 {
-    extern __shared__ int32_t hist[];       // [E]
+    extern __shared__ __align__(16) int32_t sm[];
+    int32_t *hist = sm;                      // [E]
+    int32_t *ids_s = hist + align4(E);       // [tpc * K], 16-byte aligned
     __shared__ uint32_t s_err;
-    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    const int tid = threadIdx.x;
     const int c = blockIdx.x;
     const int t0 = min(T, c * tpc), t1 = min(T, t0 + tpc);
-    const int first = t0 * K, n = (t1 - t0) * K;
+    const int m = (t1 - t0) * K;
 
     for (int e = tid; e < E; e += kThreads) hist[e] = 0;
     if (tid == 0) s_err = 0;
     __syncthreads();
     pdl_wait();
     pdl_trigger();
-
-    int lo, hi;
-    warp_segment(n, w, lo, hi);
-    uint32_t err = warp_count<true>(ids + first, lo, hi, E, lane, hist);
-    err |= check_duplicates(ids + first, t1 - t0, K, E);
-    if (err) atomicOr(&s_err, err);
+    stage_i32(ids_s, ids + (size_t)t0 * K, m);
+    cp_async_wait_all();
     __syncthreads();
 
-    for (int e = tid; e < E; e += kThreads) ws_hist[(size_t)c * E + e] = hist[e];
+    for (int i = tid; i < m; i += kThreads) {
+        const int e = ids_s[i];
+        if ((unsigned)e < (unsigned)E) atomicAdd(hist + e, 1);
+    }
+    const uint32_t err = token_errors(ids_s, t1 - t0, K, E);
+    if (err) atomicOr(&s_err, err);
+    __syncthreads();
+    for (int e = tid; e < E; e += kThreads) ws_cnt[(size_t)e * chunks + c] = hist[e];
     if (tid == 0) ws_err[c] = s_err;
 }
 
-// Ranking pass.  kFused: one block covers all T tokens and also produces the
-// counts and errors.  Otherwise block c covers chunk c and takes the counts
-// of every chunk from the workspace; block 0 writes the shared outputs.
-template <bool kFused>
-__global__ void __launch_bounds__(kThreads, 1)
-layout_rank_kernel(const int32_t *__restrict__ ids, int T, int K, int E, int R,
-                   int tpc, int chunks, const int32_t *__restrict__ ws_hist,
-                   const uint32_t *__restrict__ ws_err,
-                   int32_t *__restrict__ counts, int32_t *__restrict__ offsets,
-                   int32_t *__restrict__ rank_offsets,
-                   int32_t *__restrict__ src_token,
-                   int32_t *__restrict__ dst_row, uint32_t *__restrict__ dev_error)
+// Multi-launch path, kernel 2 (one block): per expert, the exclusive prefix
+// of the chunk histograms (in place), the totals, their exclusive scan, the
+// rank offsets and the OR of the chunks' error bits.
+__global__ void __launch_bounds__(kScanThreads)
+layout_scan_kernel(int E, int R, int chunks, int32_t *__restrict__ ws_cnt,
+                   const uint32_t *__restrict__ ws_err, int32_t *__restrict__ counts,
+                   int32_t *__restrict__ offsets, int32_t *__restrict__ rank_offsets,
+                   uint32_t *__restrict__ dev_error)
 {
-    extern __shared__ int32_t smem[];
-    int32_t *hist = smem;                    // [kWarps][E]
-    int32_t *ebase = hist + kWarps * E;      // [E + 1]
-    int32_t *warp_sums = ebase + E + 1;      // [32]
-    int32_t *part = warp_sums + 32;          // [2][kThreads], multi-block only
+    __shared__ int32_t tot[MOE_MAX_EXPERTS];
+    __shared__ int32_t off[MOE_MAX_EXPERTS + 1];
+    __shared__ int32_t warp_sums[32];
     __shared__ uint32_t s_err;
-
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-    const int c = blockIdx.x;
-    const int t0 = min(T, c * tpc), t1 = min(T, t0 + tpc);
-    const int first = t0 * K, n = (t1 - t0) * K;
-
-    for (int i = tid; i < kWarps * E; i += kThreads) hist[i] = 0;
+    constexpr int kWarpsS = kScanThreads / 32;
+    constexpr int EU = 4, CU = 4;            // experts and 32-chunk steps per batch
     if (tid == 0) s_err = 0;
     __syncthreads();
     pdl_wait();
     pdl_trigger();
 
-    // 1. per-warp counts of this block's entries
-    int lo, hi;
-    warp_segment(n, w, lo, hi);
-    uint32_t err = warp_count<false>(ids + first, lo, hi, E, lane, hist + w * E);
-    if (kFused) {
-        err |= check_duplicates(ids, T, K, E);
-        if (err) atomicOr(&s_err, err);
-    } else {
-        // totals over all chunks and over the chunks before this one,
-        // P threads per expert
-        const int P = max(1, kThreads / E);
-        const int e = tid % E, p = tid / E;
-        int tot = 0, pre = 0;
-        if (p < P)
-            for (int cc = p; cc < chunks; cc += P) {
-                const int v = __ldg(ws_hist + (size_t)cc * E + e);
-                tot += v;
-                if (cc < c) pre += v;
-            }
-        part[tid] = tot;
-        part[kThreads + tid] = pre;
+    for (int e0 = w * EU; e0 < E; e0 += kWarpsS * EU) {
+        int carry[EU];
+#pragma unroll
+        for (int i = 0; i < EU; ++i) carry[i] = 0;
+        for (int c0 = 0; c0 < chunks; c0 += 32 * CU) {
+            int v[EU][CU];
+#pragma unroll
+            for (int i = 0; i < EU; ++i)
+#pragma unroll
+                for (int j = 0; j < CU; ++j) {
+                    const int e = e0 + i, c = c0 + 32 * j + lane;
+                    v[i][j] = (e < E && c < chunks) ? ws_cnt[(size_t)e * chunks + c] : 0;
+                }
+#pragma unroll
+            for (int i = 0; i < EU; ++i)
+#pragma unroll
+                for (int j = 0; j < CU; ++j) {
+                    int x = v[i][j];
+#pragma unroll
+                    for (int d = 1; d < 32; d <<= 1) {
+                        const int y = __shfl_up_sync(kFullMask, x, d);
+                        if (lane >= d) x += y;
+                    }
+                    const int e = e0 + i, c = c0 + 32 * j + lane;
+                    if (e < E && c < chunks)
+                        ws_cnt[(size_t)e * chunks + c] = carry[i] + x - v[i][j];
+                    carry[i] += __shfl_sync(kFullMask, x, 31);
+                }
+        }
+        if (lane == 0)
+#pragma unroll
+            for (int i = 0; i < EU; ++i)
+                if (e0 + i < E) tot[e0 + i] = carry[i];
     }
+    uint32_t err = 0;
+    for (int c = tid; c < chunks; c += kScanThreads) err |= ws_err[c];
+    if (err) atomicOr(&s_err, err);
     __syncthreads();
-
-    // 2. scans: warps within the block, then experts across the block
-    int cnt = 0, prefix = 0;
-    if (tid < E) {
-        int run = 0;
-        for (int ww = 0; ww < kWarps; ++ww) {
-            const int v = hist[ww * E + tid];
-            hist[ww * E + tid] = run;
-            run += v;
-        }
-        cnt = run;
-        if (!kFused) {
-            const int P = max(1, kThreads / E);
-            int tot = 0, pre = 0;
-            for (int p = 0; p < P; ++p) {
-                tot += part[p * E + tid];
-                pre += part[kThreads + p * E + tid];
-            }
-            cnt = tot;
-            prefix = pre;
-        }
-    }
-    int total;
-    const int off = block_exclusive_scan(cnt, warp_sums, total);
-    if (tid < E) {
-        ebase[tid] = off;
-        if (c == 0) {
-            counts[tid] = cnt;
-            offsets[tid] = off;
-        }
-        for (int ww = 0; ww < kWarps; ++ww) hist[ww * E + tid] += off + prefix;
+    scan_experts<kScanThreads>(tot, off, E, warp_sums);
+    for (int e = tid; e < E; e += kScanThreads) {
+        counts[e] = tot[e];
+        offsets[e] = off[e];
     }
     if (tid == 0) {
-        ebase[E] = total;
-        if (c == 0) offsets[E] = total;
+        offsets[E] = off[E];
+        if (dev_error) *dev_error = s_err;
     }
-    __syncthreads();
-    if (c == 0) {
-        const int epr = E / R;
-        for (int r = tid; r <= R; r += kThreads) rank_offsets[r] = ebase[r * epr];
-        if (tid == 0 && dev_error) {
-            uint32_t e = s_err;
-            if (!kFused)
-                for (int cc = 0; cc < chunks; ++cc) e |= __ldg(ws_err + cc);
-            *dev_error = e;
-        }
-    }
-
-    // 3. slots, in entry order
-    for (int b = lo; b < hi; b += 32) {
-        const int i = b + lane;
-        const bool valid = i < hi;
-        const int id = valid ? __ldg(ids + first + i) : 0;
-        const bool ok = valid && (unsigned)id < (unsigned)E;
-        const unsigned m = __match_any_sync(kFullMask, ok ? id : -1 - lane);
-        if (ok) {
-            const int slot = hist[w * E + id] + __popc(m & ((1u << lane) - 1u));
-            dst_row[first + i] = slot;
-            src_token[slot] = (first + i) / K;
-        } else if (valid) {
-            dst_row[first + i] = -1;
-        }
-        __syncwarp();
-        if (ok && lane == 31 - __clz(m)) hist[w * E + id] += __popc(m);
-        __syncwarp();
-    }
+    const int epr = E / R;
+    for (int r = tid; r <= R; r += kScanThreads) rank_offsets[r] = off[r * epr];
 }
 
-size_t rank_smem_bytes(int E, bool fused)
+// Ranking.  kSelf: one launch; every block stages all T*K ids, counts the
+// totals and the entries before its chunk itself, and block 0 writes the
+// counts, offsets, rank offsets and error word.  Otherwise the block's
+// per-expert base comes from the scan kernel's offsets and prefixes.
+template <bool kSelf>
+__global__ void __launch_bounds__(kThreads)
+layout_rank_kernel(const int32_t *__restrict__ ids, int T, int K, int E, int R,
+                   int tpc, int chunks, const int32_t *__restrict__ ws_cnt,
+                   int32_t *__restrict__ counts, int32_t *__restrict__ offsets,
+                   int32_t *__restrict__ rank_offsets,
+                   int32_t *__restrict__ src_token,
+                   int32_t *__restrict__ dst_row, uint32_t *__restrict__ dev_error)
 {
-    return sizeof(int32_t) * ((size_t)kWarps * E + E + 1 + 32 + (fused ? 0 : 2 * kThreads));
+    extern __shared__ __align__(16) int32_t sm[];
+    int32_t *rows = sm;                          // [kWarps][E] running slots
+    int32_t *base = rows + kWarps * E;           // [E + 1]
+    int32_t *total = base + E + 1;               // [E]      (kSelf)
+    int32_t *before = total + E;                 // [E]      (kSelf)
+    // all entries (kSelf) or the chunk's, 16-byte aligned for the staging copy
+    int32_t *ids_s = sm + align4(kWarps * E + E + 1 + (kSelf ? 2 * E : 0));
+    __shared__ int32_t warp_sums[32];
+    __shared__ uint32_t s_err;
+
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    const int c = blockIdx.x;
+    const int t0 = min(T, c * tpc), t1 = min(T, t0 + tpc);
+    const int first = t0 * K, m = (t1 - t0) * K, n = T * K;
+
+    for (int i = tid; i < kWarps * E; i += kThreads) rows[i] = 0;
+    if (kSelf)
+        for (int e = tid; e < E; e += kThreads) total[e] = before[e] = 0;
+    if (tid == 0) s_err = 0;
+    __syncthreads();
+    pdl_wait();
+    pdl_trigger();
+    if (kSelf) {
+        stage_i32(ids_s, ids, n);
+    } else {
+        stage_i32(ids_s, ids + first, m);
+        for (int e = tid; e < E; e += kThreads)
+            base[e] = __ldg(offsets + e) + __ldg(ws_cnt + (size_t)e * chunks + c);
+    }
+    cp_async_wait_all();
+    __syncthreads();
+    const int32_t *mine = kSelf ? ids_s + first : ids_s;
+
+    if (kSelf) {
+        for (int i = tid; i < n; i += kThreads) {
+            const int e = ids_s[i];
+            if ((unsigned)e < (unsigned)E) {
+                atomicAdd(total + e, 1);
+                if (i < first) atomicAdd(before + e, 1);
+            }
+        }
+        if (c == 0) {
+            const uint32_t err = token_errors(ids_s, T, K, E);
+            if (err) atomicOr(&s_err, err);
+        }
+    }
+    int lo, hi;
+    warp_segment<kWarps>(m, w, lo, hi);
+    warp_count(mine, lo, hi, E, lane, rows + w * E);
+    __syncthreads();
+
+    if (kSelf) {
+        scan_experts<kThreads>(total, base, E, warp_sums);
+        if (c == 0) {
+            for (int e = tid; e < E; e += kThreads) {
+                counts[e] = total[e];
+                offsets[e] = base[e];
+            }
+            if (tid == 0) {
+                offsets[E] = base[E];
+                if (dev_error) *dev_error = s_err;
+            }
+            const int epr = E / R;
+            for (int r = tid; r <= R; r += kThreads) rank_offsets[r] = base[r * epr];
+        }
+    }
+    for (int e = tid; e < E; e += kThreads) {
+        int run = base[e] + (kSelf ? before[e] : 0);
+#pragma unroll
+        for (int ww = 0; ww < kWarps; ++ww) {
+            const int v = rows[ww * E + e];
+            rows[ww * E + e] = run;
+            run += v;
+        }
+    }
+    __syncthreads();
+    warp_rank(mine, lo, hi, E, K, first, lane, rows + w * E, dst_row, src_token);
+}
+
+size_t rank_smem_bytes(const LayoutPlan &p, int T, int K, int E)
+{
+    const size_t ids = p.single_launch ? (size_t)T * K : (size_t)p.tokens_per_chunk * K;
+    const int extra = p.single_launch ? 2 * E : 0;
+    return sizeof(int32_t) * ((size_t)align4(kWarps * E + E + 1 + extra) + ids);
 }
 
 // Raises a kernel's dynamic shared memory limit once per device.
@@ -276,21 +256,25 @@ cudaError_t allow_smem(const void *fn, size_t bytes)
 {
     if (bytes <= 48 * 1024) return cudaSuccess;
     static std::mutex mu;
-    static int done[2][64];
+    static const void *done_fn[8][64];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    const int which = (fn == (const void *)layout_rank_kernel<true>) ? 0 : 1;
     std::lock_guard<std::mutex> lock(mu);
-    if (dev < 64 && done[which][dev]) return cudaSuccess;
+    if (dev < 64)
+        for (auto &row : done_fn)
+            if (row[dev] == fn) return cudaSuccess;
     int max_optin = 0;
     e = cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     if (e != cudaSuccess) return e;
-    const size_t need = (size_t)sizeof(int32_t) * (kWarps * MOE_MAX_EXPERTS + MOE_MAX_EXPERTS + 1 + 32 + 2 * kThreads);
-    const int set = (int)(need < (size_t)max_optin ? need : (size_t)max_optin);
-    if ((size_t)set < bytes) return cudaErrorInvalidValue;
-    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, set);
-    if (e == cudaSuccess && dev < 64) done[which][dev] = 1;
+    if ((size_t)max_optin < bytes) return cudaErrorInvalidValue;
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, max_optin);
+    if (e == cudaSuccess && dev < 64)
+        for (auto &row : done_fn)
+            if (row[dev] == nullptr) {
+                row[dev] = fn;
+                break;
+            }
     return e;
 }
 
@@ -300,8 +284,12 @@ LayoutPlan plan_layout(int T, int K, int E)
 {
     (void)E;
     const long long n = (long long)T * K;
-    if (n <= kFusedMaxEntries) return {true, T, 1};
-    int tpc = kChunkEntries / K > 1 ? kChunkEntries / K : 1;
+    if (n <= kSelfMaxEntries) {
+        const int tpc = kSelfChunk / K > 1 ? kSelfChunk / K : 1;
+        const int chunks = T > 0 ? ceil_div(T, tpc) : 1;
+        return {true, tpc, chunks};
+    }
+    int tpc = kChunk / K > 1 ? kChunk / K : 1;
     int chunks = ceil_div(T, tpc);
     if (chunks > kMaxChunks) {
         tpc = ceil_div(T, kMaxChunks);
@@ -312,7 +300,7 @@ LayoutPlan plan_layout(int T, int K, int E)
 
 size_t layout_workspace_bytes(const LayoutPlan &plan, int E)
 {
-    if (plan.fused) return 0;
+    if (plan.single_launch) return 0;
     const size_t b = sizeof(int32_t) * (size_t)plan.chunks * ((size_t)E + 1);
     return (b + 255) & ~(size_t)255;
 }
@@ -323,31 +311,34 @@ cudaError_t launch_layout(const int32_t *topk_ids, int T, int K, int E, int R,
                           int32_t *dst_row, uint32_t *dev_error,
                           void *workspace, cudaStream_t stream)
 {
-    const LayoutPlan plan = plan_layout(T, K, E);
-    if (plan.fused) {
-        const size_t smem = rank_smem_bytes(E, true);
-        cudaError_t e = allow_smem((const void *)layout_rank_kernel<true>, smem);
+    const LayoutPlan p = plan_layout(T, K, E);
+    const size_t rsmem = rank_smem_bytes(p, T, K, E);
+    if (p.single_launch) {
+        cudaError_t e = allow_smem((const void *)layout_rank_kernel<true>, rsmem);
         if (e != cudaSuccess) return e;
-        return launch_pdl(layout_rank_kernel<true>, dim3(1), dim3(kThreads), smem,
-                          stream, topk_ids, T, K, E, R, T, 1,
-                          (const int32_t *)nullptr, (const uint32_t *)nullptr,
-                          expert_counts, expert_offsets, rank_offsets, src_token,
-                          dst_row, dev_error);
+        return launch_pdl(layout_rank_kernel<true>, dim3(p.chunks), dim3(kThreads), rsmem,
+                          stream, topk_ids, T, K, E, R, p.tokens_per_chunk, p.chunks,
+                          (const int32_t *)nullptr, expert_counts, expert_offsets,
+                          rank_offsets, src_token, dst_row, dev_error);
     }
-    int32_t *ws_hist = static_cast<int32_t *>(workspace);
-    uint32_t *ws_err = reinterpret_cast<uint32_t *>(ws_hist + (size_t)plan.chunks * E);
-    cudaError_t e = launch_pdl(layout_count_kernel, dim3(plan.chunks), dim3(kThreads),
-                               sizeof(int32_t) * E, stream, topk_ids, T, K, E,
-                               plan.tokens_per_chunk, ws_hist, ws_err);
+    int32_t *ws_cnt = static_cast<int32_t *>(workspace);
+    uint32_t *ws_err = reinterpret_cast<uint32_t *>(ws_cnt + (size_t)p.chunks * E);
+    const size_t csmem = sizeof(int32_t) * ((size_t)align4(E) + (size_t)p.tokens_per_chunk * K);
+    cudaError_t e = allow_smem((const void *)layout_count_kernel, csmem);
     if (e != cudaSuccess) return e;
-    const size_t smem = rank_smem_bytes(E, false);
-    e = allow_smem((const void *)layout_rank_kernel<false>, smem);
+    e = launch_pdl(layout_count_kernel, dim3(p.chunks), dim3(kThreads), csmem, stream,
+                   topk_ids, T, K, E, p.tokens_per_chunk, p.chunks, ws_cnt, ws_err);
     if (e != cudaSuccess) return e;
-    return launch_pdl(layout_rank_kernel<false>, dim3(plan.chunks), dim3(kThreads),
-                      smem, stream, topk_ids, T, K, E, R, plan.tokens_per_chunk,
-                      plan.chunks, (const int32_t *)ws_hist, (const uint32_t *)ws_err,
-                      expert_counts, expert_offsets, rank_offsets, src_token,
-                      dst_row, dev_error);
+    e = launch_pdl(layout_scan_kernel, dim3(1), dim3(kScanThreads), 0, stream, E, R,
+                   p.chunks, ws_cnt, (const uint32_t *)ws_err, expert_counts,
+                   expert_offsets, rank_offsets, dev_error);
+    if (e != cudaSuccess) return e;
+    e = allow_smem((const void *)layout_rank_kernel<false>, rsmem);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(layout_rank_kernel<false>, dim3(p.chunks), dim3(kThreads), rsmem,
+                      stream, topk_ids, T, K, E, R, p.tokens_per_chunk, p.chunks,
+                      (const int32_t *)ws_cnt, expert_counts, expert_offsets,
+                      rank_offsets, src_token, dst_row, dev_error);
 }
 
 }  // namespace moe

@@ -9,8 +9,9 @@
 // This kernel does both in one launch without any block waiting for another:
 //
 //  * block (t, c) packs slice c of token t's row;
-//  * before that, every block recomputes, in its own shared memory, the
-//    expert histogram of all T*K entries, the histogram of the entries that
+//  * before that, every block copies all T*K ids into its shared memory
+//    (asynchronous copies, one memory latency) and recomputes there the
+//    expert histogram of all entries, the histogram of the entries that
 //    come before token t, and the exclusive scan of the totals.  The slot of
 //    entry (t, k) is offsets[e] + (entries of e before token t) + (earlier
 //    k' of token t with the same e), the same stable order as moe_layout;
@@ -23,6 +24,7 @@
 // C ABI falls back to moe_layout + moe_dispatch otherwise.
 #include "common.cuh"
 #include "internal.h"
+#include "layout_common.cuh"
 #include "moe_layout.h"
 #include "rowops.cuh"
 
@@ -32,48 +34,6 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kMaxEntries = 8192;
 constexpr long long kMaxRedundantEntries = 1ll << 22;
-
-// Exclusive scan of hist[0..E) into off[0..E], 4 experts per thread.
-__device__ __forceinline__ void scan_experts(const int32_t *hist, int32_t *off,
-                                             int E, int32_t *warp_sums)
-{
-    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-    constexpr int kPer = MOE_MAX_EXPERTS / kThreads;
-    int v[kPer];
-    int s = 0;
-#pragma unroll
-    for (int j = 0; j < kPer; ++j) {
-        const int e = tid * kPer + j;
-        v[j] = e < E ? hist[e] : 0;
-        s += v[j];
-    }
-    int x = s;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-        const int y = __shfl_up_sync(kFullMask, x, d);
-        if (lane >= d) x += y;
-    }
-    if (lane == 31) warp_sums[w] = x;
-    __syncthreads();
-    if (w == 0) {
-        int q = lane < kThreads / 32 ? warp_sums[lane] : 0;
-#pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-            const int y = __shfl_up_sync(kFullMask, q, d);
-            if (lane >= d) q += y;
-        }
-        if (lane < kThreads / 32) warp_sums[lane] = q;
-    }
-    __syncthreads();
-    int run = (w ? warp_sums[w - 1] : 0) + x - s;
-#pragma unroll
-    for (int j = 0; j < kPer; ++j) {
-        const int e = tid * kPer + j;
-        if (e < E) off[e] = run;
-        run += v[j];
-    }
-    if (tid == 0) off[E] = warp_sums[kThreads / 32 - 1];
-}
 
 template <int KT, bool kFp8>
 __global__ void __launch_bounds__(kThreads)
@@ -85,10 +45,11 @@ layout_dispatch_kernel(const int32_t *__restrict__ ids, const uint4 *__restrict_
                        uint32_t *__restrict__ dev_error, uint8_t *__restrict__ packed,
                        float *__restrict__ scales)
 {
-    extern __shared__ int32_t sm[];
+    extern __shared__ __align__(16) int32_t sm[];
     int32_t *hist = sm;                   // [E] all entries
     int32_t *before = hist + E;           // [E] entries of tokens before t
     int32_t *off = before + E;            // [E + 1]
+    int32_t *ids_s = sm + align4(3 * E + 1);  // [T*K], 16-byte aligned
     __shared__ int32_t slots[MOE_MAX_TOPK];
     __shared__ int32_t warp_sums[32];
     __shared__ uint32_t s_err;
@@ -125,38 +86,30 @@ layout_dispatch_kernel(const int32_t *__restrict__ ids, const uint4 *__restrict_
         }
     }
 
-    uint32_t err = 0;
+    stage_i32(ids_s, ids, n);
+    cp_async_wait_all();
+    __syncthreads();
+
     for (int i = tid; i < n; i += kThreads) {
-        const int e = __ldg(ids + i);
+        const int e = ids_s[i];
         if ((unsigned)e < (unsigned)E) {
             atomicAdd(hist + e, 1);
             if (i < mine) atomicAdd(before + e, 1);
-        } else {
-            err |= MOE_DEV_ERR_EXPERT_RANGE;
         }
     }
     if (blockIdx.x == 0) {
-        for (int tt = tid; tt < T; tt += kThreads) {
-            const int32_t *row = ids + (size_t)tt * k_count;
-            for (int x = 0; x < k_count; ++x) {
-                const int ex = __ldg(row + x);
-                if ((unsigned)ex >= (unsigned)E) continue;
-                for (int y = x + 1; y < k_count; ++y)
-                    if (__ldg(row + y) == ex) err |= MOE_DEV_ERR_DUPLICATE;
-            }
-        }
+        const uint32_t err = token_errors(ids_s, T, k_count, E);
+        if (err) atomicOr(&s_err, err);
     }
-    if (err) atomicOr(&s_err, err);
     __syncthreads();
-    scan_experts(hist, off, E, warp_sums);
-    __syncthreads();
+    scan_experts<kThreads>(hist, off, E, warp_sums);
 
     if (tid < k_count) {
-        const int e = __ldg(ids + mine + tid);
+        const int e = ids_s[mine + tid];
         int slot = -1;
         if ((unsigned)e < (unsigned)E) {
             int dup = 0;
-            for (int x = 0; x < tid; ++x) dup += __ldg(ids + mine + x) == e;
+            for (int x = 0; x < tid; ++x) dup += ids_s[mine + x] == e;
             slot = off[e] + before[e] + dup;
         }
         slots[tid] = slot;
@@ -227,7 +180,7 @@ cudaError_t run_fused(const FusedPlan &p, const int32_t *ids, const void *tokens
                       int32_t *dst_row, uint32_t *dev_error, void *packed,
                       float *scales, cudaStream_t s)
 {
-    const size_t smem = sizeof(int32_t) * (3 * (size_t)E + 1);
+    const size_t smem = sizeof(int32_t) * ((size_t)align4(3 * E + 1) + (size_t)T * K);
     return launch_pdl(layout_dispatch_kernel<KT, kFp8>, dim3(T * p.chunks), dim3(kThreads),
                       smem, s, ids, static_cast<const uint4 *>(tokens), T, H, K, E, R,
                       p.chunks, p.upc, counts, offsets, rank_offsets, src_token,

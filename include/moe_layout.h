@@ -196,8 +196,8 @@ MOE_API moe_status_t moe_layout_dispatch(const int32_t *topk_ids, const void *to
                                          cudaStream_t stream);
 
 /* Number of kernel launches moe_layout_dispatch makes for these sizes: 1
- * when it runs as a single kernel, 2 or 3 otherwise (moe_layout's one or two
- * kernels, then moe_dispatch's).  0 for invalid sizes. */
+ * when it runs as a single kernel, otherwise moe_layout's one or three
+ * kernels plus moe_dispatch's one.  0 for invalid sizes. */
 MOE_API int32_t moe_layout_dispatch_kernels(int32_t T, int32_t H, int32_t K,
                                             int32_t E, int32_t fp8);
 

@@ -98,8 +98,9 @@ def test_layout_dispatch_plan_query(lib):
     # decode shapes run as one kernel, prefill shapes as layout + dispatch
     assert moe.moe_layout_dispatch_kernels(128, 7168, 8, 256, False) == 1
     assert moe.moe_layout_dispatch_kernels(256, 7168, 8, 256, True) == 1
-    assert moe.moe_layout_dispatch_kernels(4096, 7168, 8, 384, False) == 3
-    assert moe.moe_layout_dispatch_kernels(1000, 4096, 8, 128, False) == 2
+    assert moe.moe_layout_dispatch_kernels(4096, 7168, 8, 384, False) == 4
+    assert moe.moe_layout_dispatch_kernels(1000, 4096, 8, 128, False) == 4
+    assert moe.moe_layout_dispatch_kernels(512, 7168, 8, 256, False) == 2
     assert moe.moe_layout_dispatch_kernels(0, 128, 4, 16, False) == 1
     assert moe.moe_layout_dispatch_kernels(128, 100, 8, 256, False) == 0    # H % 8
     assert moe.moe_layout_dispatch_kernels(128, 136, 8, 256, True) == 0     # H % 128

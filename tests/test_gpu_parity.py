@@ -60,7 +60,8 @@ SHAPES = [  # T, K, E, R: fused single block, chunked, ragged tails, limits
     (1000, 6, 64, 8), (1024, 8, 256, 32), (1025, 8, 256, 32),
     (1500, 5, 40, 5), (4097, 2, 1024, 16), (5000, 8, 1024, 1024),
     (20000, 8, 384, 48), (70001, 4, 96, 12), (3000, 32, 64, 4),
-    (300000, 1, 1, 1),
+    (300000, 1, 1, 1), (500, 8, 256, 32), (1365, 3, 5, 5), (3000, 3, 16, 4),
+    (4096, 1, 1024, 2), (130000, 8, 128, 16),
 ]
 
 
