@@ -267,8 +267,12 @@ cudaError_t allow_smem(const void *fn, size_t bytes)
     int max_optin = 0;
     e = cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     if (e != cudaSuccess) return e;
-    if ((size_t)max_optin < bytes) return cudaErrorInvalidValue;
-    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, max_optin);
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, fn);
+    if (e != cudaSuccess) return e;
+    const size_t dyn_max = (size_t)max_optin - fa.sharedSizeBytes;
+    if (dyn_max < bytes) return cudaErrorInvalidValue;
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn_max);
     if (e == cudaSuccess && dev < 64)
         for (auto &row : done_fn)
             if (row[dev] == nullptr) {
