@@ -16,7 +16,9 @@ conversions (exhaustive decode, constructed ties for encode); the layout
 against numpy's stable argsort and brute force over all tiny routings; bf16
 dispatch by bit identity; FP8 dispatch by the closed-form error bound of the
 block scale; combine against exact rational arithmetic of the fused
-multiply-add chain and against the identity round trip.
+multiply-add chain and against the identity round trip; the FP8-input combine
+against exact rational arithmetic and against the bf16 combine wherever the
+dequantised values are exact in bf16.
 """
 from __future__ import annotations
 
@@ -78,6 +80,8 @@ def _load():
             lib.oracle_dispatch_fp8.restype = None
             lib.oracle_combine.argtypes = [P, P, P, i32, i32, i32, P]
             lib.oracle_combine.restype = None
+            lib.oracle_combine_fp8.argtypes = [P, P, P, P, i32, i32, i32, P]
+            lib.oracle_combine_fp8.restype = None
             _lib = lib
     return _lib
 
@@ -193,4 +197,21 @@ def combine(y_bits: np.ndarray, topk_weights: np.ndarray,
     H = y.shape[1]
     out = np.zeros((T, H), np.uint16)
     _load().oracle_combine(_ptr(y), _ptr(w), _ptr(d), T, H, K, _ptr(out))
+    return out
+
+
+def combine_fp8(codes: np.ndarray, scales: np.ndarray, topk_weights: np.ndarray,
+                dst_row: np.ndarray) -> np.ndarray:
+    """Weighted sum of e4m3 expert outputs: value = f32(code) * block scale,
+    then the same fp32 FMA chain in k order and one bf16 rounding."""
+    q = _c(codes, np.uint8)
+    s = _c(scales, np.float32)
+    w = _c(topk_weights, np.float32)
+    d = _c(dst_row, np.int32)
+    T, K = d.shape
+    H = q.shape[1]
+    if H % 128 or s.shape != (q.shape[0], H // 128):
+        raise ValueError("codes/scales shapes disagree (H must be a multiple of 128)")
+    out = np.zeros((T, H), np.uint16)
+    _load().oracle_combine_fp8(_ptr(q), _ptr(s), _ptr(w), _ptr(d), T, H, K, _ptr(out))
     return out

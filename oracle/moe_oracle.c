@@ -288,3 +288,35 @@ void oracle_f32_to_e4m3_n(const float *in, int64_t n, uint8_t *out)
 {
     for (int64_t i = 0; i < n; ++i) out[i] = oracle_f32_to_e4m3_satfinite(in[i]);
 }
+
+/* ------------------------------------------------------------------------ */
+/* Combine from FP8 expert outputs (codes + per-1x128-block scales).         */
+/* ------------------------------------------------------------------------ */
+
+/* The same weighted sum as oracle_combine, but each expert output element is
+ * given as an e4m3 code q and its block's fp32 scale s, the form the
+ * block-scaled FP8 dispatch produces ("Evaluation": block-scaled fp8).
+ * Reading: the element's value is the fp32 product f32(q) * s (rounded to
+ * nearest), exactly what dequantising the block means; the chain is then the
+ * same fp32 fused multiply-add in k order from +0, rounded once to bf16.
+ * codes [T*K, H] bytes, scales [T*K, H/128] fp32; H % 128 == 0. */
+void oracle_combine_fp8(const uint8_t *codes, const float *scales,
+                        const float *topk_weights, const int32_t *dst_row,
+                        int32_t T, int32_t H, int32_t K, uint16_t *out)
+{
+    int64_t rows = (int64_t)T * K;
+    int32_t nb = H / 128;
+    for (int32_t t = 0; t < T; ++t)
+        for (int32_t j = 0; j < H; ++j) {
+            float acc = 0.0f;
+            for (int32_t k = 0; k < K; ++k) {
+                int32_t r = dst_row[(int64_t)t * K + k];
+                if (r < 0 || r >= rows) continue;
+                float w = topk_weights[(int64_t)t * K + k];
+                float y = oracle_e4m3_to_f32(codes[(int64_t)r * H + j]) *
+                          scales[(int64_t)r * nb + j / 128];
+                acc = fmaf(w, y, acc);
+            }
+            out[(int64_t)t * H + j] = oracle_f32_to_bf16(acc);
+        }
+}

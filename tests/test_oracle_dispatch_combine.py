@@ -244,3 +244,108 @@ def test_per_expert_scalar_closed_form(oracle):
                     np.abs(yd[lay.dst_row]))
     err = np.abs(f32(out).astype(np.float64) - exact)
     assert np.all(err <= np.abs(exact) * 2.0 ** -8 + mag * w.K * 2.0 ** -23 + 1e-30)
+
+
+# ------------------------------------------------------ combine, FP8 input --
+
+def exact_combine_fp8(codes, scales, w, dst_row):
+    """Exact rationals: value = round_f32(f32(code) * scale), then the fp32
+    FMA chain from +0 and one bf16 rounding."""
+    T, K = dst_row.shape
+    H = codes.shape[1]
+    dec = torch.from_numpy(codes.reshape(-1)).view(torch.float8_e4m3fn).float().numpy().reshape(codes.shape)
+    out = np.zeros((T, H), np.uint16)
+    for t in range(T):
+        for j in range(H):
+            acc = Fraction(0)
+            for k in range(K):
+                r = dst_row[t, k]
+                y = _round_fraction(Fraction(float(dec[r, j])) * Fraction(float(scales[r, j // 128])), 23)
+                acc = _round_fraction(Fraction(float(w[t, k])) * y + acc, 23)
+            b = _round_fraction(acc, 7)
+            out[t, j] = 0 if b == 0 else wl.to_bf16_bits(np.array([float(b)], np.float32))[0]
+    return out
+
+
+def test_combine_fp8_exact_rational(oracle):
+    rng = np.random.default_rng(21)
+    for K in (1, 3, 8):
+        T, H = 2, 128
+        codes = rng.integers(0, 256, (T * K, H)).astype(np.uint8)
+        codes[(codes & 0x7F) == 0x7F] = 0x3C               # no NaN codes
+        scales = (rng.random((T * K, 1)) * np.exp2(rng.integers(-20, 20, (T * K, 1)))).astype(np.float32)
+        w = rng.standard_normal((T, K)).astype(np.float32)
+        dst = rng.permutation(T * K).astype(np.int32).reshape(T, K)
+        got = oracle.combine_fp8(codes, scales, w, dst)
+        assert np.array_equal(got, exact_combine_fp8(codes, scales, w, dst)), K
+
+
+def test_combine_fp8_equals_bf16_combine_when_exact(oracle):
+    """With power-of-two scales the dequantised values are exact in bf16, so
+    the FP8-input combine equals the (pinned) bf16 combine of those values."""
+    rng = np.random.default_rng(22)
+    T, H, K = 16, 256, 4
+    codes = rng.integers(0, 256, (T * K, H)).astype(np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x40
+    scales = np.exp2(rng.integers(-10, 10, (T * K, H // 128))).astype(np.float32)
+    w = rng.standard_normal((T, K)).astype(np.float32)
+    dst = rng.permutation(T * K).astype(np.int32).reshape(T, K)
+    dec = torch.from_numpy(codes.reshape(-1)).view(torch.float8_e4m3fn).float().numpy().reshape(codes.shape)
+    y = wl.to_bf16_bits(dec * np.repeat(scales, 128, axis=1))
+    assert np.array_equal(f32(y), dec * np.repeat(scales, 128, axis=1))   # exact
+    assert np.array_equal(oracle.combine_fp8(codes, scales, w, dst), oracle.combine(y, w, dst))
+
+
+def test_combine_fp8_round_trip(oracle):
+    """FP8 dispatch then FP8-input combine returns x within the block bound."""
+    w = wl.get("prefill_qwen3")
+    inp = wl.make_inputs(w, T=24)
+    lay = oracle.layout(inp.topk_ids, w.E, w.R)
+    codes, scales = oracle.dispatch_fp8(inp.tokens, lay.dst_row)
+    out = f32(oracle.combine_fp8(codes, scales, inp.topk_weights, lay.dst_row)).astype(np.float64)
+    x = f32(inp.tokens).astype(np.float64).reshape(24, -1, 128)
+    amax = np.abs(x).max(axis=2, keepdims=True)
+    err = np.abs(out.reshape(24, -1, 128) - x)
+    assert np.all(err <= amax / 28 * 1.01 + np.abs(x) * 2.0 ** -7)
+
+
+def test_combine_fp8_rounding_sensitive(oracle):
+    """Token i: w_i * (q_i * s_i) - 1 * (q_i * 1) with w_i, s_i = 1 + small
+    multiples of 2^-23: the result is a few fp32 ulps of q_i, exact in bf16,
+    so it shows whether the value is round(q*s) before the FMA (the reading)
+    or the scale folded into the weight, or the product left unrounded."""
+    dec = torch.from_numpy(np.arange(256, dtype=np.uint8)).view(torch.float8_e4m3fn).float().numpy()
+    cases = []
+    for code in range(0x38, 0x40):                      # 1 + m/8, m = 0..7
+        for a in range(-6, 7):
+            for b in range(-6, 7):
+                w = np.float32(1 + a * 2.0 ** -23)
+                s = np.float32(1 + b * 2.0 ** -23)
+                q = np.float32(dec[code])
+                reading = np.float32(w * np.float32(q * s))
+                folded = np.float32(np.float32(w * s) * q)
+                exact = np.float32(float(w) * float(q) * float(s))
+                cases.append((code, w, s, reading != folded or reading != exact))
+    assert sum(c[3] for c in cases) >= 20               # the set separates the orders
+    T, H, K = len(cases), 128, 2
+    codes = np.zeros((T * K, H), np.uint8)
+    scales = np.ones((T * K, 1), np.float32)
+    wts = np.zeros((T, K), np.float32)
+    dst = np.arange(T * K, dtype=np.int32).reshape(T, K)
+    for i, (code, w, s, _) in enumerate(cases):
+        codes[2 * i] = code
+        codes[2 * i + 1] = code
+        scales[2 * i] = s
+        wts[i] = (w, -1.0)
+    got = oracle.combine_fp8(codes, scales, wts, dst)
+    assert np.array_equal(got, got[:, :1].repeat(H, 1))  # every column is the same sum
+    for i in range(T):                                   # column 0, exact rationals
+        acc = Fraction(0)
+        for k in range(K):
+            y = _round_fraction(Fraction(float(dec[codes[2 * i + k, 0]])) *
+                                Fraction(float(scales[2 * i + k, 0])), 23)
+            acc = _round_fraction(Fraction(float(wts[i, k])) * y + acc, 23)
+        b = _round_fraction(acc, 7)
+        e = 0 if b == 0 else wl.to_bf16_bits(np.array([float(b)], np.float32))[0]
+        assert got[i, 0] == e, i
+    assert np.count_nonzero(got[:, 0]) > T // 2        # outputs carry the low bits
