@@ -61,6 +61,9 @@ def parse_args(argv=None):
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--unfused", action="store_true",
                    help="moe_layout + moe_dispatch as two calls instead of moe_layout_dispatch")
+    p.add_argument("--combine", choices=("bf16", "fp8"), default="bf16",
+                   help="fp8: combine reads the FP8 dispatch output directly "
+                        "(moe_combine_fp8, identity experts); needs --dispatch fp8")
     return p.parse_args(argv)
 
 
@@ -115,13 +118,14 @@ def algorithmic_bytes(w, dispatch: str):
     else:
         disp = 2 * T * H + T * K * H + 4 * T * K * (H // 128) + 4 * T * K
     comb = 2 * T * K * H + 8 * T * K + 2 * T * H
-    return {"layout": layout, "dispatch": disp, "combine": comb,
+    comb8 = T * K * H + 4 * T * K * (H // 128) + 8 * T * K + 2 * T * H
+    return {"layout": layout, "dispatch": disp, "combine": comb, "combine_fp8": comb8,
             "layout_dispatch": layout + disp - 4 * T * K}
 
 
 def kernel_source_hash(kernel: str) -> str:
     srcs = {"layout": ["layout.cu"], "dispatch": ["dispatch.cu", "rowops.cuh"],
-            "combine": ["combine.cu"],
+            "combine": ["combine.cu"], "combine_fp8": ["combine.cu"],
             "layout_dispatch": ["layout_dispatch.cu", "rowops.cuh", "layout.cu",
                                 "dispatch.cu"]}[kernel]
     h = hashlib.sha256()
@@ -296,9 +300,15 @@ class BufferSet:
         import torch
         import combine_moe_layout_05_gb300 as moe
         T, H, K = w.T, w.H, w.K
-        self.tokens = torch.from_numpy(inp.tokens.view(np.int16)).to(device).view(torch.bfloat16)
-        self.ids = torch.from_numpy(inp.topk_ids).to(device)
-        self.weights = torch.from_numpy(inp.topk_weights).to(device)
+        # the step's inputs sit in one contiguous buffer, so a host upload is
+        # one copy: [tokens | ids | weights], each part 256-byte aligned
+        self.input_layout = input_layout(w)
+        self.inputs = torch.empty(self.input_layout["bytes"], dtype=torch.uint8, device=device)
+        self.inputs.copy_(torch.from_numpy(pack_inputs(w, inp)))
+        o = self.input_layout
+        self.tokens = self.inputs[o["tokens"]:o["tokens"] + 2 * T * H].view(torch.bfloat16).view(T, H)
+        self.ids = self.inputs[o["ids"]:o["ids"] + 4 * T * K].view(torch.int32).view(T, K)
+        self.weights = self.inputs[o["weights"]:o["weights"] + 4 * T * K].view(torch.float32).view(T, K)
         self.layout = moe.LayoutBuffers(T, K, w.E, w.R, device=device)
         if dispatch == "bf16":
             self.packed = torch.empty((T * K, H), dtype=torch.bfloat16, device=device)
@@ -311,10 +321,29 @@ class BufferSet:
         self.out = torch.empty((T, H), dtype=torch.bfloat16, device=device)
 
     def nbytes(self):
-        ts = [self.tokens, self.ids, self.weights, self.packed, self.out,
+        ts = [self.inputs, self.packed, self.out,
               self.layout.src_token, self.layout.dst_row]
         ts += [t for t in (self.scales, self.y) if t is not None]
         return sum(t.numel() * t.element_size() for t in ts)
+
+
+def input_layout(w):
+    """Byte offsets of tokens, ids and weights in one input buffer."""
+    al = lambda x: (x + 255) // 256 * 256
+    tok = 0
+    ids = al(2 * w.T * w.H)
+    wts = al(ids + 4 * w.T * w.K)
+    return {"tokens": tok, "ids": ids, "weights": wts, "bytes": al(wts + 4 * w.T * w.K)}
+
+
+def pack_inputs(w, inp):
+    import numpy as np
+    o = input_layout(w)
+    buf = np.zeros(o["bytes"], np.uint8)
+    for name, arr in (("tokens", inp.tokens), ("ids", inp.topk_ids), ("weights", inp.topk_weights)):
+        b = np.ascontiguousarray(arr).view(np.uint8).ravel()
+        buf[o[name]:o[name] + b.size] = b
+    return buf
 
 
 def expert_outputs(w, dispatch, inp, buf):
@@ -333,7 +362,7 @@ def expert_outputs(w, dispatch, inp, buf):
     return y.view(torch.int16).cpu().numpy().view("uint16")
 
 
-def step_ops(moe, dispatch, unfused=False):
+def step_ops(moe, dispatch, unfused=False, combine="bf16"):
     """The calls of one step, as (name, fn(buffer_set)) in launch order."""
     fp8 = dispatch == "fp8"
     if unfused:
@@ -343,12 +372,16 @@ def step_ops(moe, dispatch, unfused=False):
     else:
         ops = [("layout_dispatch", lambda b: b.layout.run_dispatch(
             b.ids, b.tokens, b.packed, b.scales, fp8=fp8))]
-    ops.append(("combine", lambda b: moe.moe_combine(b.y, b.weights, b.layout.dst_row, b.out)))
+    if combine == "fp8":
+        ops.append(("combine_fp8", lambda b: moe.moe_combine_fp8(
+            b.packed, b.scales, b.weights, b.layout.dst_row, b.out)))
+    else:
+        ops.append(("combine", lambda b: moe.moe_combine(b.y, b.weights, b.layout.dst_row, b.out)))
     return ops
 
 
-def run_step(moe, buf, dispatch, unfused=False):
-    for _, fn in step_ops(moe, dispatch, unfused):
+def run_step(moe, buf, dispatch, unfused=False, combine="bf16"):
+    for _, fn in step_ops(moe, dispatch, unfused, combine):
         fn(buf)
 
 
@@ -360,7 +393,7 @@ def capture(torch, steps_fn, n_steps):
     return g
 
 
-def check_parity(w, dispatch, inp, buf):
+def check_parity(w, dispatch, inp, buf, combine="bf16"):
     """The bench's own gate: one step of set 0 against the oracle."""
     import numpy as np
     import torch
@@ -375,13 +408,16 @@ def check_parity(w, dispatch, inp, buf):
         ec, es = oracle.dispatch_fp8(inp.tokens, ref.dst_row)
         ok &= np.array_equal(buf.packed.view(torch.uint8).cpu().numpy(), ec)
         ok &= np.array_equal(buf.scales.cpu().numpy().view(np.uint32), es.view(np.uint32))
-    y = buf.y.view(torch.int16).cpu().numpy().view(np.uint16)
-    exp_out = oracle.combine(y, inp.topk_weights, ref.dst_row)
+    if combine == "fp8":
+        exp_out = oracle.combine_fp8(ec, es, inp.topk_weights, ref.dst_row)
+    else:
+        y = buf.y.view(torch.int16).cpu().numpy().view(np.uint16)
+        exp_out = oracle.combine(y, inp.topk_weights, ref.dst_row)
     ok &= np.array_equal(buf.out.view(torch.int16).cpu().numpy().view(np.uint16), exp_out)
     return "bit-exact" if ok else "MISMATCH"
 
 
-def time_oracle(w, dispatch, inp, y_bits, seconds: float, max_tokens=None):
+def time_oracle(w, dispatch, inp, y_bits, seconds: float, max_tokens=None, combine="bf16"):
     """Oracle steps (layout + dispatch + combine) on the host until `seconds`
     have passed; returns (tokens/s, tokens per step, steps)."""
     import oracle
@@ -393,8 +429,11 @@ def time_oracle(w, dispatch, inp, y_bits, seconds: float, max_tokens=None):
         if dispatch == "bf16":
             oracle.dispatch_bf16(x, ref.dst_row)
         else:
-            oracle.dispatch_fp8(x, ref.dst_row)
-        oracle.combine(y_bits[: T * w.K], wts, ref.dst_row)
+            codes, scales = oracle.dispatch_fp8(x, ref.dst_row)
+        if combine == "fp8":
+            oracle.combine_fp8(codes, scales, wts, ref.dst_row)
+        else:
+            oracle.combine(y_bits[: T * w.K], wts, ref.dst_row)
         n += 1
         el = time.perf_counter() - t0
         if el >= seconds:
@@ -450,7 +489,9 @@ def run_ours(args):
     w = wl.get(args.workload or wl.HEADLINE)
     dispatch = args.dispatch or w.dispatch[0]
     inp = wl.make_inputs(w, seed=shard_seed(w.seed, rank))
-    ops = step_ops(moe, dispatch, args.unfused)
+    if args.combine == "fp8" and dispatch != "fp8":
+        raise SystemExit("--combine fp8 needs FP8 dispatch (--dispatch fp8)")
+    ops = step_ops(moe, dispatch, args.unfused, args.combine)
 
     # rotating buffer sets: total >= 3x L2, so every step starts cold in L2
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
@@ -459,18 +500,18 @@ def run_ours(args):
     if args.unfused:
         ops[1][1](first)
     torch.cuda.synchronize()
-    y_bits = expert_outputs(w, dispatch, inp, first)
-    per_set = first.nbytes() + y_bits.nbytes
+    y_bits = expert_outputs(w, dispatch, inp, first) if args.combine == "bf16" else None
+    per_set = first.nbytes() + (0 if y_bits is None else y_bits.nbytes)
     n_sets = max(2, math.ceil(3 * l2 / per_set))
     sets = [BufferSet(w, dispatch, inp, y_bits, device) for _ in range(n_sets)]
     del first
     for b in sets:                       # eager pass: attributes, parity data
-        run_step(moe, b, dispatch, args.unfused)
+        run_step(moe, b, dispatch, args.unfused, args.combine)
     torch.cuda.synchronize()
 
     K = args.steps
     G = max(n_sets, (min(args.graph_steps, max(K, 1)) // n_sets) * n_sets)
-    step = lambda b: run_step(moe, b, dispatch, args.unfused)
+    step = lambda b: run_step(moe, b, dispatch, args.unfused, args.combine)
     g = capture(torch, lambda m, sh: [step(sets[j % n_sets]) for j in range(m)], G)
     rem = K % G
     gr = capture(torch, lambda m, sh: [step(sets[j % n_sets]) for j in range(m)], rem) if rem else None
@@ -479,7 +520,7 @@ def run_ours(args):
     for j in range(args.warmup % G):
         step(sets[j % n_sets])
     torch.cuda.synchronize()
-    parity = check_parity(w, dispatch, inp, sets[-1]) if rank == 0 else None
+    parity = check_parity(w, dispatch, inp, sets[-1], args.combine) if rank == 0 else None
 
     sampler = ClockSampler(local)
     sampler.start()
@@ -523,7 +564,7 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline and world == 1:
-        tps, tsamp, nst = time_oracle(w, dispatch, inp, y_bits, args.cpu_seconds)
+        tps, tsamp, nst = time_oracle(w, dispatch, inp, y_bits, args.cpu_seconds, combine=args.combine)
         cpu = {"value": round(tps, 1), "unit": "tokens/s", "cores": 1, "kind": "oracle",
                "sample": f"{nst} oracle steps of the full {w.name} batch "
                          f"(T={tsamp}), single thread, {args.cpu_seconds:.0f} s budget"}
@@ -536,7 +577,9 @@ def run_ours(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": w.name, "T": w.T, "H": w.H, "E": w.E, "R": w.R,
-                   "K": w.K, "dispatch": dispatch, "combine": "bf16 in, f32 accumulate",
+                   "K": w.K, "dispatch": dispatch,
+                   "combine": ("e4m3 + block scales in (identity experts)" if args.combine == "fp8"
+                               else "bf16 in") + ", f32 accumulate",
                    "experts": w.experts, "routing": w.routing,
                    "calls": [n for n, _ in ops],
                    "l2": f"{n_sets} rotating buffer sets, {n_sets * per_set / 1e6:.0f} MB "
@@ -570,31 +613,52 @@ def launches_per_step(w, dispatch, unfused) -> int:
 
 
 def run_e2e(args, w, dispatch, inp, sets, n_sets, device, torch, moe, drv):
-    """Same steps through host buffers: page-locked H2D copies of tokens, ids
-    and weights, the three calls, and a D2H copy of the output, all inside the
-    timed region."""
+    """The same steps through host buffers, as a serving loop runs them: each
+    step copies its tokens, ids and weights (one contiguous buffer) from
+    page-locked host memory,
+    runs the calls, and copies its output back to page-locked host memory,
+    all inside the timed region.  Copies and compute sit on three streams
+    (host-to-device, compute, device-to-host) so step j+1's upload and step
+    j-1's download overlap step j's kernels; events order each buffer set's
+    reuse (an upload waits for the compute that last read the set, a compute
+    waits for the download that last read its output)."""
     import numpy as np
+    packed_in = pack_inputs(w, inp)
+    h2d = packed_in.nbytes
+    d2h = w.T * w.H * 2
     host = []
     for _ in range(n_sets):
-        h = {}
-        for name, arr in (("tokens", inp.tokens), ("ids", inp.topk_ids),
-                          ("weights", inp.topk_weights)):
-            addr, view = drv.pinned(arr.nbytes)
-            view[:] = np.ascontiguousarray(arr).view(np.uint8).ravel()
-            h[name] = (addr, arr.nbytes)
-        h["out"] = drv.pinned(w.T * w.H * 2)[0]
-        host.append(h)
-    h2d = sum(host[0][k][1] for k in ("tokens", "ids", "weights"))
-    d2h = w.T * w.H * 2
+        addr, view = drv.pinned(h2d)
+        view[:] = packed_in
+        host.append({"inputs": addr, "out": drv.pinned(d2h)[0]})
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
 
     def body(n, sh):
+        comp = torch.cuda.current_stream()
+        up.wait_stream(comp)                  # fork the side streams into the capture
+        down.wait_stream(comp)
+        comp_done, down_done = {}, {}
         for j in range(n):
             b, h = sets[j % n_sets], host[j % n_sets]
-            drv.h2d(b.tokens.data_ptr(), *h["tokens"], sh)
-            drv.h2d(b.ids.data_ptr(), *h["ids"], sh)
-            drv.h2d(b.weights.data_ptr(), *h["weights"], sh)
-            run_step(moe, b, dispatch, args.unfused)
-            drv.d2h(h["out"], b.out.data_ptr(), d2h, sh)
+            with torch.cuda.stream(up):
+                if j - n_sets in comp_done:   # the set's previous compute has read it
+                    up.wait_event(comp_done[j - n_sets])
+                drv.h2d(b.inputs.data_ptr(), h["inputs"], h2d, up.cuda_stream)
+                up_done = torch.cuda.Event()
+                up_done.record(up)
+            comp.wait_event(up_done)
+            if j - n_sets in down_done:       # the set's previous output was read
+                comp.wait_event(down_done[j - n_sets])
+            run_step(moe, b, dispatch, args.unfused, args.combine)
+            comp_done[j] = torch.cuda.Event()
+            comp_done[j].record(comp)
+            with torch.cuda.stream(down):
+                down.wait_event(comp_done[j])
+                drv.d2h(h["out"], b.out.data_ptr(), d2h, down.cuda_stream)
+                down_done[j] = torch.cuda.Event()
+                down_done[j].record(down)
+        comp.wait_stream(up)                  # join
+        comp.wait_stream(down)
 
     K = args.steps
     G = max(n_sets, (min(args.graph_steps, max(K, 1)) // n_sets) * n_sets)
@@ -623,7 +687,8 @@ def run_e2e(args, w, dispatch, inp, sets, n_sets, device, torch, moe, drv):
     same = np.array_equal(out0, sets[0].out.view(torch.uint8).cpu().numpy().ravel())
     return {"value": round(world * w.T * K / (ms * 1e-3), 1), "unit": "tokens/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "ms_per_step": round(ms / K, 6), "output_matches_device_run": bool(same)}
+            "ms_per_step": round(ms / K, 6), "output_matches_device_run": bool(same),
+            "pipeline": "H2D, compute and D2H on three streams, overlapping across steps"}
 
 
 # ------------------------------------------------------- reference (oracle) --
@@ -639,21 +704,23 @@ def run_reference(args):
     dispatch = args.dispatch or w.dispatch[0]
     inp = wl.make_inputs(w)
     ref = oracle.layout(inp.topk_ids, w.E, w.R)
-    if dispatch == "bf16":
+    if args.combine == "fp8":
+        y_bits = None
+    elif dispatch == "bf16":
         y_bits = oracle.dispatch_bf16(inp.tokens, ref.dst_row)
     else:
         y_bits = wl.random_rows(w.T * w.K, w.H, inp.expert_rows_seed)
     # size each step so the whole run stays within about 90 s of host time
     t0 = time.perf_counter()
-    time_oracle(w, dispatch, inp, y_bits, 0.0)
+    time_oracle(w, dispatch, inp, y_bits, 0.0, combine=args.combine)
     full = time.perf_counter() - t0
     budget = 90.0 / max(1, args.steps + args.warmup)
     T_s = max(1, min(w.T, int(w.T * budget / max(full, 1e-9))))
     for _ in range(args.warmup):
-        time_oracle(w, dispatch, inp, y_bits, 0.0, max_tokens=T_s)
+        time_oracle(w, dispatch, inp, y_bits, 0.0, max_tokens=T_s, combine=args.combine)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        time_oracle(w, dispatch, inp, y_bits, 0.0, max_tokens=T_s)
+        time_oracle(w, dispatch, inp, y_bits, 0.0, max_tokens=T_s, combine=args.combine)
     el = time.perf_counter() - t0
     value = T_s * args.steps / el
     sample = (f"each step: oracle layout + {dispatch} dispatch + combine on the first "

@@ -8,7 +8,8 @@ dispatch and combine.
 """
 from ._binding import (MOE_DEV_ERR_DUPLICATE, MOE_DEV_ERR_EXPERT_RANGE,
                        LayoutBuffers, MoeError, declared_functions,
-                       library_path, load, moe_combine, moe_dispatch,
+                       library_path, load, moe_combine, moe_combine_fp8,
+                       moe_dispatch,
                        moe_layout, moe_layout_dispatch,
                        moe_layout_dispatch_kernels,
                        moe_layout_workspace_bytes,
@@ -17,6 +18,7 @@ from ._binding import (MOE_DEV_ERR_DUPLICATE, MOE_DEV_ERR_EXPERT_RANGE,
 __all__ = [
     "MOE_DEV_ERR_DUPLICATE", "MOE_DEV_ERR_EXPERT_RANGE", "LayoutBuffers",
     "MoeError", "declared_functions", "library_path", "load", "moe_combine",
+    "moe_combine_fp8",
     "moe_dispatch", "moe_layout", "moe_layout_dispatch", "moe_layout_dispatch_kernels",
     "moe_layout_workspace_bytes",
     "moe_status_string",

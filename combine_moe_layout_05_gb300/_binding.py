@@ -62,6 +62,8 @@ def load(path: str | None = None):
             lib.moe_layout_dispatch.restype = ctypes.c_int
             lib.moe_layout_dispatch_kernels.argtypes = [i32, i32, i32, i32, i32]
             lib.moe_layout_dispatch_kernels.restype = i32
+            lib.moe_combine_fp8.argtypes = [P, P, P, P, i32, i32, i32, P, P]
+            lib.moe_combine_fp8.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -209,6 +211,24 @@ def moe_combine(expert_out, topk_weights, dst_row, out, stream=None) -> None:
     st = load().moe_combine(_ptr(expert_out), _ptr(topk_weights), _ptr(dst_row),
                             T, H, K, _ptr(out), _stream(stream))
     _raise("moe_combine", st)
+
+
+def moe_combine_fp8(expert_out, expert_scales, topk_weights, dst_row, out,
+                    stream=None) -> None:
+    """Routing-weighted sum of e4m3 expert rows (value = code * block scale)."""
+    T, K = topk_weights.shape
+    H = out.shape[1]
+    _check("expert_out", expert_out, torch.float8_e4m3fn)
+    _check("expert_scales", expert_scales, torch.float32)
+    _check("topk_weights", topk_weights, torch.float32)
+    _check("dst_row", dst_row, torch.int32)
+    _check("out", out, torch.bfloat16)
+    if dst_row.numel() != T * K or out.shape[0] != T or expert_out.numel() < T * K * H \
+            or expert_scales.numel() < T * K * (H // 128):
+        raise ValueError("moe_combine_fp8: argument sizes disagree")
+    st = load().moe_combine_fp8(_ptr(expert_out), _ptr(expert_scales), _ptr(topk_weights),
+                                _ptr(dst_row), T, H, K, _ptr(out), _stream(stream))
+    _raise("moe_combine_fp8", st)
 
 
 class LayoutBuffers:

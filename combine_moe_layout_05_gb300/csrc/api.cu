@@ -15,7 +15,8 @@ bool layout_sizes_ok(int32_t T, int32_t K, int32_t E)
 {
     if (T < 0 || E < 1 || E > MOE_MAX_EXPERTS) return false;
     if (K < 1 || K > MOE_MAX_TOPK || K > E) return false;
-    return (int64_t)T * K <= (int64_t)INT32_MAX - 1;
+    if ((int64_t)T * K > (int64_t)INT32_MAX - 1) return false;
+    return moe::layout_supported(T, K, E);
 }
 
 moe_status_t rows_ok(int32_t T, int32_t H, int32_t K)
@@ -105,6 +106,24 @@ moe_status_t moe_combine(const void *expert_out, const float *topk_weights,
         return MOE_ERR_ALIGNMENT;
     return cuda_status(moe::launch_combine(expert_out, topk_weights, dst_row, T,
                                            H, K, out, stream));
+}
+
+moe_status_t moe_combine_fp8(const void *expert_out, const float *expert_scales,
+                             const float *topk_weights, const int32_t *dst_row,
+                             int32_t T, int32_t H, int32_t K, void *out,
+                             cudaStream_t stream)
+{
+    moe_status_t s = rows_ok(T, H, K);
+    if (s != MOE_OK) return s;
+    if (H % 128 != 0) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;
+    if (!expert_out || !expert_scales || !topk_weights || !dst_row || !out)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned(expert_out, 16) || !aligned(out, 16) || !aligned(expert_scales, 4) ||
+        !aligned(topk_weights, 4) || !aligned(dst_row, 4))
+        return MOE_ERR_ALIGNMENT;
+    return cuda_status(moe::launch_combine_fp8(expert_out, expert_scales, topk_weights,
+                                               dst_row, T, H, K, out, stream));
 }
 
 moe_status_t moe_layout_dispatch(const int32_t *topk_ids, const void *tokens,

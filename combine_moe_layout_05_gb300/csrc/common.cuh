@@ -5,6 +5,7 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 namespace moe {
 
@@ -48,6 +49,15 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2_satfinite(float lo, float hi)
     uint16_t r;
     asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
     return r;
+}
+
+// Two e4m3 codes (low byte first) widened exactly to fp32 via f16x2.
+__device__ __forceinline__ float2 e4m3x2_to_f32x2(uint16_t codes)
+{
+    uint32_t h;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(codes));
+    __half2 v = *reinterpret_cast<__half2 *>(&h);
+    return __half22float2(v);
 }
 
 __host__ __device__ constexpr int ceil_div(int a, int b) { return (a + b - 1) / b; }

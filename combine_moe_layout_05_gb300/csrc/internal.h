@@ -16,6 +16,8 @@ struct LayoutPlan {
 };
 
 LayoutPlan plan_layout(int T, int K, int E);
+// False when a batch this large would not fit the kernels' shared memory.
+bool layout_supported(int T, int K, int E);
 size_t layout_workspace_bytes(const LayoutPlan &plan, int E);
 
 cudaError_t launch_layout(const int32_t *topk_ids, int T, int K, int E, int R,
@@ -35,6 +37,10 @@ cudaError_t launch_dispatch_fp8(const void *tokens, int T, int H, int K,
 cudaError_t launch_combine(const void *expert_out, const float *topk_weights,
                            const int32_t *dst_row, int T, int H, int K,
                            void *out, cudaStream_t stream);
+
+cudaError_t launch_combine_fp8(const void *codes, const float *scales,
+                               const float *topk_weights, const int32_t *dst_row,
+                               int T, int H, int K, void *out, cudaStream_t stream);
 
 // Layout and dispatch together: one fused kernel when
 // layout_dispatch_fused() says the batch is small enough, else the layout

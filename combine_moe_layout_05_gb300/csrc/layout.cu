@@ -24,8 +24,9 @@
 // all T*K ids and counts the totals and the entries before its chunk itself.
 // Larger batches take three launches and a workspace, with no block ever
 // waiting for another: a counting kernel writes each chunk's histogram, a
-// one-block kernel turns the histograms into per-chunk prefixes and the
-// expert offsets, and the ranking kernel assigns the slots.
+// one-block kernel turns the histograms into each chunk's first slot per
+// expert and writes the expert offsets, and the ranking kernel assigns the
+// slots.
 #include "common.cuh"
 #include "internal.h"
 #include "layout_common.cuh"
@@ -41,11 +42,11 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kSelfMaxEntries = 4096;
 constexpr int kSelfChunk = 512;
 constexpr int kChunk = 1024;
-constexpr int kMaxChunks = 16384;
+constexpr int kScanCells = 40 * 1024;    // chunks x E staged by the scan (160 KB)
 constexpr int kScanThreads = 1024;
 
 // Multi-launch path, kernel 1: histogram and error bits of chunk c.
-// ws_cnt is expert-major: ws_cnt[e * chunks + c].
+// ws_cnt is chunk-major: ws_cnt[c * E + e].
 __global__ void __launch_bounds__(kThreads)
 layout_count_kernel(const int32_t *__restrict__ ids, int T, int K, int E, int tpc,
                     int chunks, int32_t *__restrict__ ws_cnt,
@@ -76,73 +77,73 @@ layout_count_kernel(const int32_t *__restrict__ ids, int T, int K, int E, int tp
     const uint32_t err = token_errors(ids_s, t1 - t0, K, E);
     if (err) atomicOr(&s_err, err);
     __syncthreads();
-    for (int e = tid; e < E; e += kThreads) ws_cnt[(size_t)e * chunks + c] = hist[e];
+    for (int e = tid; e < E; e += kThreads) ws_cnt[(size_t)c * E + e] = hist[e];
     if (tid == 0) ws_err[c] = s_err;
 }
 
-// Multi-launch path, kernel 2 (one block): per expert, the exclusive prefix
-// of the chunk histograms (in place), the totals, their exclusive scan, the
-// rank offsets and the OR of the chunks' error bits.
+// Multi-launch path, kernel 2 (one block): turns the chunk histograms into
+// each chunk's first slot per expert, in place:
+//     ws_cnt[c * E + e] <- offsets[e] + sum of ws_cnt[c' * E + e], c' < c
+// and writes the counts, offsets, rank offsets and the OR of the error bits.
+// The histograms are staged in shared memory (one memory latency); P
+// threads share each expert's chunks, and the threads of a warp hold
+// consecutive experts, so shared-memory accesses never conflict.
 __global__ void __launch_bounds__(kScanThreads)
 layout_scan_kernel(int E, int R, int chunks, int32_t *__restrict__ ws_cnt,
                    const uint32_t *__restrict__ ws_err, int32_t *__restrict__ counts,
                    int32_t *__restrict__ offsets, int32_t *__restrict__ rank_offsets,
                    uint32_t *__restrict__ dev_error)
 {
+    extern __shared__ __align__(16) int32_t cnt[];   // [chunks][E]
+    __shared__ int32_t part[kScanThreads];           // [P][E] partial sums, then prefixes
     __shared__ int32_t tot[MOE_MAX_EXPERTS];
     __shared__ int32_t off[MOE_MAX_EXPERTS + 1];
     __shared__ int32_t warp_sums[32];
     __shared__ uint32_t s_err;
-    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-    constexpr int kWarpsS = kScanThreads / 32;
-    constexpr int EU = 4, CU = 4;            // experts and 32-chunk steps per batch
+    const int tid = threadIdx.x;
+    const int P = E < kScanThreads ? kScanThreads / E : 1;
+    const int e = tid % E, p = tid / E;
+    const bool mine = p < P;
+    const int per = ceil_div(chunks, P);
+    const int c0 = min(chunks, p * per), c1 = min(chunks, c0 + per);
     if (tid == 0) s_err = 0;
     __syncthreads();
     pdl_wait();
     pdl_trigger();
-
-    for (int e0 = w * EU; e0 < E; e0 += kWarpsS * EU) {
-        int carry[EU];
-#pragma unroll
-        for (int i = 0; i < EU; ++i) carry[i] = 0;
-        for (int c0 = 0; c0 < chunks; c0 += 32 * CU) {
-            int v[EU][CU];
-#pragma unroll
-            for (int i = 0; i < EU; ++i)
-#pragma unroll
-                for (int j = 0; j < CU; ++j) {
-                    const int e = e0 + i, c = c0 + 32 * j + lane;
-                    v[i][j] = (e < E && c < chunks) ? ws_cnt[(size_t)e * chunks + c] : 0;
-                }
-#pragma unroll
-            for (int i = 0; i < EU; ++i)
-#pragma unroll
-                for (int j = 0; j < CU; ++j) {
-                    int x = v[i][j];
-#pragma unroll
-                    for (int d = 1; d < 32; d <<= 1) {
-                        const int y = __shfl_up_sync(kFullMask, x, d);
-                        if (lane >= d) x += y;
-                    }
-                    const int e = e0 + i, c = c0 + 32 * j + lane;
-                    if (e < E && c < chunks)
-                        ws_cnt[(size_t)e * chunks + c] = carry[i] + x - v[i][j];
-                    carry[i] += __shfl_sync(kFullMask, x, 31);
-                }
-        }
-        if (lane == 0)
-#pragma unroll
-            for (int i = 0; i < EU; ++i)
-                if (e0 + i < E) tot[e0 + i] = carry[i];
-    }
+    stage_i32(cnt, ws_cnt, E * chunks);
     uint32_t err = 0;
     for (int c = tid; c < chunks; c += kScanThreads) err |= ws_err[c];
     if (err) atomicOr(&s_err, err);
+    cp_async_wait_all();
+    __syncthreads();
+
+    int sum = 0;
+    if (mine)
+        for (int c = c0; c < c1; ++c) sum += cnt[c * E + e];
+    if (mine) part[p * E + e] = sum;
+    __syncthreads();
+    if (tid < E) {
+        int run = 0;
+        for (int q = 0; q < P; ++q) {
+            const int v = part[q * E + tid];
+            part[q * E + tid] = run;
+            run += v;
+        }
+        tot[tid] = run;
+    }
     __syncthreads();
     scan_experts<kScanThreads>(tot, off, E, warp_sums);
-    for (int e = tid; e < E; e += kScanThreads) {
-        counts[e] = tot[e];
-        offsets[e] = off[e];
+    if (mine) {
+        int run = off[e] + part[p * E + e];
+        for (int c = c0; c < c1; ++c) {
+            const int v = cnt[c * E + e];
+            ws_cnt[(size_t)c * E + e] = run;
+            run += v;
+        }
+    }
+    for (int x = tid; x < E; x += kScanThreads) {
+        counts[x] = tot[x];
+        offsets[x] = off[x];
     }
     if (tid == 0) {
         offsets[E] = off[E];
@@ -191,8 +192,7 @@ layout_rank_kernel(const int32_t *__restrict__ ids, int T, int K, int E, int R,
         stage_i32(ids_s, ids, n);
     } else {
         stage_i32(ids_s, ids + first, m);
-        for (int e = tid; e < E; e += kThreads)
-            base[e] = __ldg(offsets + e) + __ldg(ws_cnt + (size_t)e * chunks + c);
+        for (int e = tid; e < E; e += kThreads) base[e] = __ldg(ws_cnt + (size_t)c * E + e);
     }
     cp_async_wait_all();
     __syncthreads();
@@ -251,19 +251,22 @@ size_t rank_smem_bytes(const LayoutPlan &p, int T, int K, int E)
     return sizeof(int32_t) * ((size_t)align4(kWarps * E + E + 1 + extra) + ids);
 }
 
-// Raises a kernel's dynamic shared memory limit once per device.
+// Raises a kernel's dynamic shared memory limit to the most the device
+// allows next to the kernel's static shared memory, once per device, and
+// checks that `bytes` fits.
 cudaError_t allow_smem(const void *fn, size_t bytes)
 {
-    if (bytes <= 48 * 1024) return cudaSuccess;
     static std::mutex mu;
     static const void *done_fn[8][64];
+    static size_t done_bytes[64][8];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     std::lock_guard<std::mutex> lock(mu);
     if (dev < 64)
         for (auto &row : done_fn)
-            if (row[dev] == fn) return cudaSuccess;
+            if (row[dev] == fn) return bytes <= done_bytes[dev][&row - done_fn] ? cudaSuccess
+                                                                                 : cudaErrorInvalidValue;
     int max_optin = 0;
     e = cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     if (e != cudaSuccess) return e;
@@ -277,6 +280,7 @@ cudaError_t allow_smem(const void *fn, size_t bytes)
         for (auto &row : done_fn)
             if (row[dev] == nullptr) {
                 row[dev] = fn;
+                done_bytes[dev][&row - done_fn] = dyn_max;
                 break;
             }
     return e;
@@ -293,13 +297,28 @@ LayoutPlan plan_layout(int T, int K, int E)
         const int chunks = T > 0 ? ceil_div(T, tpc) : 1;
         return {true, tpc, chunks};
     }
+    // chunks of kChunk entries, fewer (larger) when the scan's staged
+    // histograms (chunks x E ints) would not fit kScanCells
     int tpc = kChunk / K > 1 ? kChunk / K : 1;
     int chunks = ceil_div(T, tpc);
-    if (chunks > kMaxChunks) {
-        tpc = ceil_div(T, kMaxChunks);
+    const int max_chunks = kScanCells / E;
+    if (chunks > max_chunks) {
+        tpc = ceil_div(T, max_chunks);
         chunks = ceil_div(T, tpc);
     }
     return {false, tpc, chunks};
+}
+
+bool layout_supported(int T, int K, int E)
+{
+    // every kernel's dynamic shared memory must fit next to its static part
+    constexpr size_t kLimit = 200 * 1024;
+    const LayoutPlan p = plan_layout(T, K, E);
+    if (rank_smem_bytes(p, T, K, E) > kLimit) return false;
+    if (p.single_launch) return true;
+    const size_t count = sizeof(int32_t) * ((size_t)align4(E) + (size_t)p.tokens_per_chunk * K);
+    const size_t scan = sizeof(int32_t) * (size_t)E * p.chunks;
+    return count <= kLimit && scan <= kLimit;
 }
 
 size_t layout_workspace_bytes(const LayoutPlan &plan, int E)
@@ -333,7 +352,10 @@ cudaError_t launch_layout(const int32_t *topk_ids, int T, int K, int E, int R,
     e = launch_pdl(layout_count_kernel, dim3(p.chunks), dim3(kThreads), csmem, stream,
                    topk_ids, T, K, E, p.tokens_per_chunk, p.chunks, ws_cnt, ws_err);
     if (e != cudaSuccess) return e;
-    e = launch_pdl(layout_scan_kernel, dim3(1), dim3(kScanThreads), 0, stream, E, R,
+    const size_t ssmem = sizeof(int32_t) * (size_t)E * p.chunks;
+    e = allow_smem((const void *)layout_scan_kernel, ssmem);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(layout_scan_kernel, dim3(1), dim3(kScanThreads), ssmem, stream, E, R,
                    p.chunks, ws_cnt, (const uint32_t *)ws_err, expert_counts,
                    expert_offsets, rank_offsets, dev_error);
     if (e != cudaSuccess) return e;

@@ -10,18 +10,20 @@
 //
 //  * block (t, c) packs slice c of token t's row;
 //  * before that, every block copies all T*K ids into its shared memory
-//    (asynchronous copies, one memory latency) and recomputes there the
-//    expert histogram of all entries, the histogram of the entries that
-//    come before token t, and the exclusive scan of the totals.  The slot of
-//    entry (t, k) is offsets[e] + (entries of e before token t) + (earlier
-//    k' of token t with the same e), the same stable order as moe_layout;
+//    (asynchronous copies, one memory latency) and counts there, for each of
+//    its token's K entries (t, k) with expert e, the valid ids below e (that
+//    is offsets[e]), the entries of e before token t and the earlier k' of
+//    token t with id e; their sum is the slot, the same stable order as
+//    moe_layout.  One pass over the ids with K predicated counters per
+//    thread and one block reduction; no histogram, no scan, no atomics;
 //  * the row slice is loaded before the histogram work, so the HBM latency
 //    of the token row overlaps it;
-//  * slice 0 of each token writes its dst_row / src_token entries and block
-//    0 writes the counts, offsets, rank offsets and error word.
-// The redundant histogram costs T*K shared-memory atomics per block, so this
-// path is used only while blocks x entries stays small (decode shapes); the
-// C ABI falls back to moe_layout + moe_dispatch otherwise.
+//  * slice 0 of each token writes its dst_row / src_token entries; block b
+//    also counts expert b (count and offset, and the rank offset when b
+//    starts a rank), and block 0 writes the error word.
+// Each block reads all T*K ids, so this path is used only while blocks x
+// entries stays small (decode shapes); the C ABI falls back to moe_layout +
+// moe_dispatch otherwise.
 #include "common.cuh"
 #include "internal.h"
 #include "layout_common.cuh"
@@ -35,6 +37,28 @@ constexpr int kThreads = 256;
 constexpr int kMaxEntries = 8192;
 constexpr long long kMaxRedundantEntries = 1ll << 22;
 
+// Sum over the block of N per-thread counters; the totals land in out[0..N)
+// (shared memory) and are visible to every thread on return.
+template <int N>
+__device__ __forceinline__ void block_sum(const int (&v)[N], int32_t (*red)[16],
+                                          int32_t *out)
+{
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+#pragma unroll
+    for (int j = 0; j < N; ++j) {
+        const int s = __reduce_add_sync(kFullMask, v[j]);
+        if (lane == 0) red[w][j] = s;
+    }
+    __syncthreads();
+    if (threadIdx.x < N) {
+        int s = 0;
+#pragma unroll
+        for (int q = 0; q < kThreads / 32; ++q) s += red[q][threadIdx.x];
+        out[threadIdx.x] = s;
+    }
+    __syncthreads();
+}
+
 template <int KT, bool kFp8>
 __global__ void __launch_bounds__(kThreads)
 layout_dispatch_kernel(const int32_t *__restrict__ ids, const uint4 *__restrict__ tokens,
@@ -45,92 +69,121 @@ layout_dispatch_kernel(const int32_t *__restrict__ ids, const uint4 *__restrict_
                        uint32_t *__restrict__ dev_error, uint8_t *__restrict__ packed,
                        float *__restrict__ scales)
 {
-    extern __shared__ __align__(16) int32_t sm[];
-    int32_t *hist = sm;                   // [E] all entries
-    int32_t *before = hist + E;           // [E] entries of tokens before t
-    int32_t *off = before + E;            // [E + 1]
-    int32_t *ids_s = sm + align4(3 * E + 1);  // [T*K], 16-byte aligned
+    extern __shared__ __align__(16) int32_t ids_s[];   // [T*K]
+    __shared__ int32_t red[kThreads / 32][16];
+    __shared__ int32_t sums[16];
     __shared__ int32_t slots[MOE_MAX_TOPK];
-    __shared__ int32_t warp_sums[32];
     __shared__ uint32_t s_err;
 
     const int tid = threadIdx.x;
-    const int t = blockIdx.x / chunks, c = blockIdx.x - (blockIdx.x / chunks) * chunks;
+    const int nb = gridDim.x, b = blockIdx.x;
+    const int t = b / chunks, c = b - (b / chunks) * chunks;
     const int k_count = KT > 0 ? KT : K;
     const int n = T * k_count;
     const int mine = t * k_count;
     const int units = kFp8 ? (H >> 4) : (H >> 3);
     const int u0 = c * upc, u1 = min(units, u0 + upc);
     const size_t vrow = (size_t)(H >> 3);
+    const int epr = E / R;
 
-    for (int e = tid; e < E; e += kThreads) {
-        hist[e] = 0;
-        before[e] = 0;
-    }
     if (tid == 0) s_err = 0;
-    __syncthreads();
     pdl_wait();
     pdl_trigger();
 
     // the first piece of this thread's share of the row, loaded early
-    uint4 a = make_uint4(0, 0, 0, 0), b = make_uint4(0, 0, 0, 0);
+    uint4 a = make_uint4(0, 0, 0, 0), bv = make_uint4(0, 0, 0, 0);
     {
         const int u = u0 + tid;
         if (u < u1) {
             if (kFp8) {
                 a = ld_stream_v4(tokens + (size_t)t * vrow + 2 * u);
-                b = ld_stream_v4(tokens + (size_t)t * vrow + 2 * u + 1);
+                bv = ld_stream_v4(tokens + (size_t)t * vrow + 2 * u + 1);
             } else {
                 a = ld_stream_v4(tokens + (size_t)t * vrow + u);
             }
         }
     }
-
     stage_i32(ids_s, ids, n);
     cp_async_wait_all();
     __syncthreads();
 
-    for (int i = tid; i < n; i += kThreads) {
-        const int e = ids_s[i];
-        if ((unsigned)e < (unsigned)E) {
-            atomicAdd(hist + e, 1);
-            if (i < mine) atomicAdd(before + e, 1);
+    // Slots of this token's entries, 8 at a time:
+    //   slot(t,k) = #{valid ids < e} + #{entries before token t with id e}
+    //             + #{k' < k of token t with id e},  e = ids[t,k].
+    // The first pass also gives block b the count and offset of expert b
+    // (offsets[e] = #{valid ids < e}), so these outputs are spread over the
+    // grid; experts beyond the grid take further passes below.
+    for (int k0 = 0; k0 < k_count; k0 += 8) {
+        int tg[8], v[10];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            tg[j] = k0 + j < k_count ? ids_s[mine + k0 + j] : -1;
+            v[j] = 0;
         }
+        const int role = (k0 == 0 && b <= E) ? b : -1;
+        v[8] = v[9] = 0;
+        for (int i = tid; i < n; i += kThreads) {
+            const int x = ids_s[i];
+            if ((unsigned)x >= (unsigned)E) continue;
+            const bool before = i < mine;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j] += (x < tg[j]) | ((x == tg[j]) & before);
+            v[8] += x < role;
+            v[9] += x == role;
+        }
+        block_sum<10>(v, red, sums);
+        if (tid < 8 && k0 + tid < k_count) {
+            const int e = ids_s[mine + k0 + tid];
+            int slot = -1;
+            if ((unsigned)e < (unsigned)E) {
+                int dup = 0;
+                for (int x = 0; x < k0 + tid; ++x) dup += ids_s[mine + x] == e;
+                slot = sums[tid] + dup;
+            }
+            slots[k0 + tid] = slot;
+            if (c == 0) {
+                dst_row[mine + k0 + tid] = slot;
+                if (slot >= 0) src_token[slot] = t;
+            }
+        }
+        if (role >= 0 && tid == 0) {
+            offsets[role] = sums[8];
+            if (role < E) counts[role] = sums[9];
+            if (role % epr == 0) rank_offsets[role / epr] = sums[8];
+        }
+        __syncthreads();    // sums is reused by the next pass
     }
-    if (blockIdx.x == 0) {
+    // experts not covered by the first pass (grids smaller than E + 1)
+    for (int r0 = b + nb; r0 <= E; r0 += 8 * nb) {
+        int v[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] = 0;
+        for (int i = tid; i < n; i += kThreads) {
+            const int x = ids_s[i];
+            if ((unsigned)x >= (unsigned)E) continue;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                v[2 * j] += x < r0 + j * nb;
+                v[2 * j + 1] += x == r0 + j * nb;
+            }
+        }
+        block_sum<16>(v, red, sums);
+        if (tid < 8) {
+            const int e = r0 + tid * nb;
+            if (e <= E) {
+                offsets[e] = sums[2 * tid];
+                if (e < E) counts[e] = sums[2 * tid + 1];
+                if (e % epr == 0) rank_offsets[e / epr] = sums[2 * tid];
+            }
+        }
+        __syncthreads();
+    }
+    if (b == 0) {
         const uint32_t err = token_errors(ids_s, T, k_count, E);
         if (err) atomicOr(&s_err, err);
+        __syncthreads();
+        if (tid == 0 && dev_error) *dev_error = s_err;
     }
-    __syncthreads();
-    scan_experts<kThreads>(hist, off, E, warp_sums);
-
-    if (tid < k_count) {
-        const int e = ids_s[mine + tid];
-        int slot = -1;
-        if ((unsigned)e < (unsigned)E) {
-            int dup = 0;
-            for (int x = 0; x < tid; ++x) dup += ids_s[mine + x] == e;
-            slot = off[e] + before[e] + dup;
-        }
-        slots[tid] = slot;
-        if (c == 0) {
-            dst_row[mine + tid] = slot;
-            if (slot >= 0) src_token[slot] = t;
-        }
-    }
-    if (blockIdx.x == 0) {
-        for (int e = tid; e < E; e += kThreads) {
-            counts[e] = hist[e];
-            offsets[e] = off[e];
-        }
-        if (tid == 0) {
-            offsets[E] = off[E];
-            if (dev_error) *dev_error = s_err;
-        }
-        const int epr = E / R;
-        for (int r = tid; r <= R; r += kThreads) rank_offsets[r] = off[r * epr];
-    }
-    __syncthreads();
 
     const int rows = n;
     for (int base = u0; base < u1; base += kThreads) {     // uniform per block
@@ -139,13 +192,13 @@ layout_dispatch_kernel(const int32_t *__restrict__ ids, const uint4 *__restrict_
         if (base != u0 && active) {
             if (kFp8) {
                 a = ld_stream_v4(tokens + (size_t)t * vrow + 2 * u);
-                b = ld_stream_v4(tokens + (size_t)t * vrow + 2 * u + 1);
+                bv = ld_stream_v4(tokens + (size_t)t * vrow + 2 * u + 1);
             } else {
                 a = ld_stream_v4(tokens + (size_t)t * vrow + u);
             }
         }
         if (kFp8) {
-            const Fp8Piece p = quantize16(a, b);    // every lane takes part
+            const Fp8Piece p = quantize16(a, bv);   // every lane takes part
             if (active)
                 store_fp8_to_slots<KT>(slots, k_count, rows, packed, scales, H, u, p);
         } else if (active) {
@@ -180,7 +233,7 @@ cudaError_t run_fused(const FusedPlan &p, const int32_t *ids, const void *tokens
                       int32_t *dst_row, uint32_t *dev_error, void *packed,
                       float *scales, cudaStream_t s)
 {
-    const size_t smem = sizeof(int32_t) * ((size_t)align4(3 * E + 1) + (size_t)T * K);
+    const size_t smem = sizeof(int32_t) * (size_t)T * K;
     return launch_pdl(layout_dispatch_kernel<KT, kFp8>, dim3(T * p.chunks), dim3(kThreads),
                       smem, s, ids, static_cast<const uint4 *>(tokens), T, H, K, E, R,
                       p.chunks, p.upc, counts, offsets, rank_offsets, src_token,

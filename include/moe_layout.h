@@ -95,7 +95,9 @@ MOE_API size_t moe_layout_workspace_bytes(int32_t T, int32_t K, int32_t E);
  *
  * topk_ids     [T,K] int32, 4-byte aligned.
  * T >= 0, 1 <= K <= min(E, MOE_MAX_TOPK), 1 <= E <= MOE_MAX_EXPERTS,
- * R >= 1 with E % R == 0, T*K < 2^31.
+ * R >= 1 with E % R == 0, T*K < 2^31, and T*K small enough for the kernels'
+ * shared memory: at least 1.6 * 10^9 / E entries (1.6 M for E = 1024,
+ * 13 M for E = 128); larger batches return MOE_ERR_INVALID_ARG.
  * Outputs (int32, 4-byte aligned): expert_counts, expert_offsets,
  * rank_offsets, src_token, dst_row.  dst_row and src_token may be NULL only
  * when T == 0.
@@ -170,6 +172,31 @@ MOE_API moe_status_t moe_dispatch(const void *tokens, int32_t T, int32_t H, int3
 MOE_API moe_status_t moe_combine(const void *expert_out, const float *topk_weights,
                          const int32_t *dst_row, int32_t T, int32_t H,
                          int32_t K, void *out, cudaStream_t stream);
+
+/*
+ * moe_combine_fp8 -- moe_combine for expert outputs held as block-scaled e4m3.
+ *
+ * The evaluated setting dispatches block-scaled FP8 ("Evaluation"); when the
+ * expert outputs stay in that form (e4m3 codes plus one fp32 scale per 1x128
+ * block, as moe_dispatch with fp8 == 1 writes them), combine can read them
+ * directly, moving about half the bytes of a bf16 combine.  Each value is
+ * y = f32(code) * scale (fp32, round to nearest), then the same chain:
+ *
+ *   acc = +0;  for k = 0 .. K-1:  acc = fma(topk_weights[t,k], y[dst_row[t,k], j], acc)
+ *   out[t, j] = bf16 round-to-nearest-even(acc)
+ *
+ * Terms whose dst_row is outside [0, T*K) are skipped.
+ *
+ * expert_out     [T*K,H] e4m3 bytes, 16-byte aligned.
+ * expert_scales  [T*K,H/128] fp32, 4-byte aligned.
+ * topk_weights   [T,K] fp32.   dst_row [T,K] int32.
+ * out            [T,H] bf16, 16-byte aligned.
+ * H >= 128 with H % 128 == 0.  T == 0 is a no-op.
+ */
+MOE_API moe_status_t moe_combine_fp8(const void *expert_out, const float *expert_scales,
+                                     const float *topk_weights, const int32_t *dst_row,
+                                     int32_t T, int32_t H, int32_t K, void *out,
+                                     cudaStream_t stream);
 
 /*
  * moe_layout_dispatch -- moe_layout followed by moe_dispatch, as one call.

@@ -120,3 +120,24 @@ def test_layout_dispatch_host_checks(lib):
     assert f(*args(packed=FAKE + 4)) == 2
     assert f(*args(fp8=1, scales=FAKE + 2)) == 2
     assert f(*args(T=4096, H=7168, K=8, E=384, R=48)) == 4       # needs workspace
+
+
+def test_layout_size_limit(lib):
+    # the shared-memory bound of the kernels: at least 1.6e9 / E entries
+    for E in (128, 384, 1024):
+        T = int(1.6e9 / E) // 8
+        assert moe.moe_layout_workspace_bytes(T, 8, E) > 0
+    assert moe.moe_layout_workspace_bytes(2_000_000, 8, 1024) == 0      # too large
+    assert _layout(lib, T=2_000_000, K=8, E=1024, R=1) == 1
+
+
+def test_combine_fp8_host_checks(lib):
+    c = lib.moe_combine_fp8
+    args = lambda **kw: [P(kw.get("q", FAKE)), P(kw.get("s", FAKE)), P(FAKE), P(FAKE),
+                         kw.get("T", 4), kw.get("H", 256), kw.get("K", 2), P(kw.get("o", FAKE)), None]
+    assert c(*args(H=200)) == 1                  # H % 128
+    assert c(*args(K=0)) == 1
+    assert c(*args(q=FAKE + 8)) == 2
+    assert c(*args(s=FAKE + 2)) == 2
+    assert c(*args(o=FAKE + 4)) == 2
+    assert c(None, None, None, None, 0, 256, 2, None, None) == 0   # T == 0: no-op
