@@ -11,7 +11,7 @@ from ._binding import (MOE_DEV_ERR_DUPLICATE, MOE_DEV_ERR_EXPERT_RANGE,
                        library_path, load, moe_combine, moe_combine_fp8,
                        moe_dispatch,
                        moe_layout, moe_layout_dispatch,
-                       moe_layout_dispatch_kernels,
+                       moe_layout_dispatch_kernels, moe_layout_static,
                        moe_layout_workspace_bytes,
                        moe_status_string)
 
@@ -19,7 +19,7 @@ __all__ = [
     "MOE_DEV_ERR_DUPLICATE", "MOE_DEV_ERR_EXPERT_RANGE", "LayoutBuffers",
     "MoeError", "declared_functions", "library_path", "load", "moe_combine",
     "moe_combine_fp8",
-    "moe_dispatch", "moe_layout", "moe_layout_dispatch", "moe_layout_dispatch_kernels",
+    "moe_dispatch", "moe_layout", "moe_layout_dispatch", "moe_layout_dispatch_kernels", "moe_layout_static",
     "moe_layout_workspace_bytes",
     "moe_status_string",
 ]

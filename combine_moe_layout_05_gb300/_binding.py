@@ -64,6 +64,8 @@ def load(path: str | None = None):
             lib.moe_layout_dispatch_kernels.restype = i32
             lib.moe_combine_fp8.argtypes = [P, P, P, P, i32, i32, i32, P, P]
             lib.moe_combine_fp8.restype = ctypes.c_int
+            lib.moe_layout_static.argtypes = [P, i32, i32, i32, i32, P, P, P, P, P, P, P]
+            lib.moe_layout_static.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -211,6 +213,30 @@ def moe_combine(expert_out, topk_weights, dst_row, out, stream=None) -> None:
     st = load().moe_combine(_ptr(expert_out), _ptr(topk_weights), _ptr(dst_row),
                             T, H, K, _ptr(out), _stream(stream))
     _raise("moe_combine", st)
+
+
+def moe_layout_static(topk_ids, E: int, R: int, expert_counts, expert_offsets,
+                      rank_offsets, src_token, dst_row, dev_error=None,
+                      stream=None) -> None:
+    """moe_layout for callers that cannot allocate: the large-batch scratch is
+    a fixed array inside the library (see include/moe_layout.h)."""
+    T, K = topk_ids.shape
+    _check("topk_ids", topk_ids, torch.int32)
+    for n, t in (("expert_counts", expert_counts), ("expert_offsets", expert_offsets),
+                 ("rank_offsets", rank_offsets), ("src_token", src_token),
+                 ("dst_row", dst_row)):
+        _check(n, t, torch.int32)
+    if expert_counts.numel() < E or expert_offsets.numel() < E + 1 or rank_offsets.numel() < R + 1:
+        raise ValueError("moe_layout_static: output arrays too small")
+    if src_token.numel() < T * K or dst_row.numel() < T * K:
+        raise ValueError("moe_layout_static: src_token/dst_row too small")
+    if dev_error is not None:
+        _check("dev_error", dev_error, torch.int32)
+    st = load().moe_layout_static(_ptr(topk_ids), T, K, E, R, _ptr(expert_counts),
+                                  _ptr(expert_offsets), _ptr(rank_offsets),
+                                  _ptr(src_token), _ptr(dst_row), _ptr(dev_error),
+                                  _stream(stream))
+    _raise("moe_layout_static", st)
 
 
 def moe_combine_fp8(expert_out, expert_scales, topk_weights, dst_row, out,

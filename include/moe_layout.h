@@ -13,10 +13,12 @@
  *
  * Conventions for every call:
  *  - All pointers are device pointers unless stated otherwise.  The caller
- *    allocates and owns every buffer; the library allocates nothing, keeps no
- *    state between calls and never synchronises.
- *  - Every call is asynchronous on `stream` (0 = legacy default stream) and
- *    may be captured into a CUDA graph.
+ *    allocates and owns every buffer; the library allocates nothing and
+ *    never synchronises, and apart from moe_layout_static's scratch array
+ *    (described with that call) it keeps no state between calls.
+ *  - moe_layout, moe_dispatch, moe_combine, moe_combine_fp8 and
+ *    moe_layout_dispatch are asynchronous on `stream` (0 = legacy default
+ *    stream) and may be captured into a CUDA graph.
  *  - Arguments are checked on the host before anything is enqueued.  A
  *    failed check returns an error status and enqueues nothing.
  *  - Matrices are row-major and dense: a [rows, H] matrix has row stride H.
@@ -227,6 +229,43 @@ MOE_API moe_status_t moe_layout_dispatch(const int32_t *topk_ids, const void *to
  * kernels plus moe_dispatch's one.  0 for invalid sizes. */
 MOE_API int32_t moe_layout_dispatch_kernels(int32_t T, int32_t H, int32_t K,
                                             int32_t E, int32_t fp8);
+
+/* Bytes of the fixed scratch array that moe_layout_static uses (256 KiB). */
+#define MOE_LAYOUT_STATIC_SCRATCH_BYTES (256u << 10)
+
+/*
+ * moe_layout_static -- moe_layout for callers that cannot allocate device
+ * memory.  (The paper has no counterpart; this is a library convenience.)
+ *
+ * Some callers cannot call cudaMalloc where they need the layout: a plugin or
+ * custom op run by an inference engine whose memory planner owns every device
+ * allocation, or a latency-critical serving loop that must not enter the
+ * device allocator once it runs (an allocation can block, synchronise or
+ * fail).  This
+ * call takes the same arguments and gives the same results as moe_layout, but
+ * has no workspace argument: the scratch that large batches need lives in a
+ * fixed array of MOE_LAYOUT_STATIC_SCRATCH_BYTES in the library's own device
+ * memory, which every GPU that loads the library keeps until the process
+ * exits.  The call allocates nothing (no cudaMalloc, no cudaFree).
+ *
+ * - Limit: a batch whose moe_layout_workspace_bytes(T,K,E) exceeds
+ *   MOE_LAYOUT_STATIC_SCRATCH_BYTES is rejected with MOE_ERR_WORKSPACE.
+ *   That covers every batch moe_layout accepts with E >= 2; with E = 1,
+ *   batches above about 33 million entries are rejected.
+ * - Set-up: the first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress, with that device current); make that first call
+ *   before any stream capture.  Set-up failure returns MOE_ERR_CUDA.
+ * - Sharing: all calls on a device share the one array, and it keeps the last
+ *   call's contents.  Nothing in it needs to start at zero: each call writes
+ *   every scratch entry before reading it.  Calls that can run at the same
+ *   time on the GPU (different streams with no ordering between them) race
+ *   on the array; order them on one stream or with events.
+ */
+MOE_API moe_status_t moe_layout_static(const int32_t *topk_ids, int32_t T, int32_t K,
+                                       int32_t E, int32_t R, int32_t *expert_counts,
+                                       int32_t *expert_offsets, int32_t *rank_offsets,
+                                       int32_t *src_token, int32_t *dst_row,
+                                       uint32_t *dev_error, cudaStream_t stream);
 
 #ifdef __cplusplus
 }
