@@ -82,6 +82,8 @@ def _load():
             lib.oracle_combine.restype = None
             lib.oracle_combine_fp8.argtypes = [P, P, P, P, i32, i32, i32, P]
             lib.oracle_combine_fp8.restype = None
+            lib.oracle_combine_rank_partial.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, P]
+            lib.oracle_combine_rank_partial.restype = None
             _lib = lib
     return _lib
 
@@ -214,4 +216,23 @@ def combine_fp8(codes: np.ndarray, scales: np.ndarray, topk_weights: np.ndarray,
         raise ValueError("codes/scales shapes disagree (H must be a multiple of 128)")
     out = np.zeros((T, H), np.uint16)
     _load().oracle_combine_fp8(_ptr(q), _ptr(s), _ptr(w), _ptr(d), T, H, K, _ptr(out))
+    return out
+
+
+def combine_rank_partial(y_bits: np.ndarray, topk_weights: np.ndarray,
+                         topk_ids: np.ndarray, dst_row: np.ndarray, E: int,
+                         R: int) -> np.ndarray:
+    """Sender-side partial sums: per destination rank an fp32 FMA chain in k
+    order rounded to bf16, then the receiver's fp32 sum in rank order."""
+    y = _c(y_bits, np.uint16)
+    w = _c(topk_weights, np.float32)
+    ids = _c(topk_ids, np.int32)
+    d = _c(dst_row, np.int32)
+    T, K = d.shape
+    H = y.shape[1]
+    if R <= 0 or E % R:
+        raise ValueError("E must be a positive multiple of R")
+    out = np.zeros((T, H), np.uint16)
+    _load().oracle_combine_rank_partial(_ptr(y), _ptr(w), _ptr(ids), _ptr(d), T, H, K,
+                                        E, R, _ptr(out))
     return out

@@ -320,3 +320,46 @@ void oracle_combine_fp8(const uint8_t *codes, const float *scales,
             out[(int64_t)t * H + j] = oracle_f32_to_bf16(acc);
         }
 }
+
+/* ------------------------------------------------------------------------ */
+/* Combine with sender-side partial sums (per destination rank).            */
+/* ------------------------------------------------------------------------ */
+
+/* The page contrasts its receiver-side accumulation with DeepEP, which sums
+ * in the sender to cut the bytes transferred and may lose accuracy doing so
+ * ("Evaluation").  Reading of that scheme on the same data:
+ *  - the sender is the rank r = e / (E/R) that hosts expert e;
+ *  - for each token, each rank forms the partial sum of its own entries as
+ *    the fp32 fused multiply-add chain over them in k order, from +0, and
+ *    rounds it to bf16 (the transfer format) -- the accuracy loss;
+ *  - the receiver adds the partials as fp32, in ascending rank order, from
+ *    +0, and rounds the total to bf16.
+ * Entries with an invalid expert id or dst_row are skipped.  With R == 1, or
+ * one entry per token, this equals oracle_combine. */
+void oracle_combine_rank_partial(const uint16_t *y, const float *topk_weights,
+                                 const int32_t *topk_ids, const int32_t *dst_row,
+                                 int32_t T, int32_t H, int32_t K, int32_t E,
+                                 int32_t R, uint16_t *out)
+{
+    int64_t rows = (int64_t)T * K;
+    int32_t per_rank = E / R;
+    for (int32_t t = 0; t < T; ++t)
+        for (int32_t j = 0; j < H; ++j) {
+            float total = 0.0f;
+            for (int32_t r = 0; r < R; ++r) {
+                float part = 0.0f;
+                int any = 0;
+                for (int32_t k = 0; k < K; ++k) {
+                    int32_t e = topk_ids[(int64_t)t * K + k];
+                    int32_t row = dst_row[(int64_t)t * K + k];
+                    if (e < 0 || e >= E || row < 0 || row >= rows) continue;
+                    if (e / per_rank != r) continue;
+                    part = fmaf(topk_weights[(int64_t)t * K + k],
+                                oracle_bf16_to_f32(y[(int64_t)row * H + j]), part);
+                    any = 1;
+                }
+                if (any) total = total + oracle_bf16_to_f32(oracle_f32_to_bf16(part));
+            }
+            out[(int64_t)t * H + j] = oracle_f32_to_bf16(total);
+        }
+}

@@ -349,3 +349,106 @@ def test_combine_fp8_rounding_sensitive(oracle):
         e = 0 if b == 0 else wl.to_bf16_bits(np.array([float(b)], np.float32))[0]
         assert got[i, 0] == e, i
     assert np.count_nonzero(got[:, 0]) > T // 2        # outputs carry the low bits
+
+
+# ----------------------------------------- combine, sender-side partial sums --
+
+def exact_rank_partial(y_bits, w, ids, dst_row, E, R):
+    """Exact rationals of the reading: per rank an fp32 FMA chain in k order
+    from +0 rounded to bf16, then the fp32 add chain over ranks in ascending
+    order from +0 and a final bf16 rounding."""
+    T, K = dst_row.shape
+    H = y_bits.shape[1]
+    yf = f32(y_bits)
+    out = np.zeros((T, H), np.uint16)
+    for t in range(T):
+        ranks = sorted({int(ids[t, k]) // (E // R) for k in range(K)})
+        for j in range(H):
+            total = Fraction(0)
+            for r in ranks:
+                part = Fraction(0)
+                for k in range(K):
+                    if int(ids[t, k]) // (E // R) == r:
+                        part = _round_fraction(Fraction(float(w[t, k])) * Fraction(float(yf[dst_row[t, k], j])) + part, 23)
+                total = _round_fraction(total + _round_fraction(part, 7), 23)
+            b = _round_fraction(total, 7)
+            out[t, j] = 0 if b == 0 else wl.to_bf16_bits(np.array([float(b)], np.float32))[0]
+    return out
+
+
+def test_rank_partial_exact_rational(oracle):
+    rng = np.random.default_rng(41)
+    for (T, K, E, R) in [(3, 4, 8, 2), (2, 8, 16, 4), (4, 3, 6, 3), (2, 6, 12, 12)]:
+        H = 8
+        ids = np.stack([rng.permutation(E)[:K] for _ in range(T)]).astype(np.int32)
+        lay = oracle.layout(ids, E, R)
+        y = wl.to_bf16_bits((rng.standard_normal((T * K, H)) *
+                             np.exp2(rng.integers(-6, 6, (T * K, H)))).astype(np.float32))
+        w = rng.standard_normal((T, K)).astype(np.float32)
+        got = oracle.combine_rank_partial(y, w, ids, lay.dst_row, E, R)
+        assert np.array_equal(got, exact_rank_partial(y, w, ids, lay.dst_row, E, R)), (T, K, E, R)
+
+
+def test_rank_partial_reduces_to_combine(oracle):
+    """One rank (R = 1), or one entry per token: no intermediate rounding is
+    added, so the result is the (pinned) receiver-side combine's."""
+    w = wl.get("decode_dsv3")
+    inp = wl.make_inputs(w, T=32)
+    for R in (1,):
+        lay = oracle.layout(inp.topk_ids, w.E, R)
+        y = oracle.dispatch_bf16(inp.tokens, lay.dst_row)
+        assert np.array_equal(oracle.combine_rank_partial(y, inp.topk_weights, inp.topk_ids, lay.dst_row, w.E, R),
+                              oracle.combine(y, inp.topk_weights, lay.dst_row))
+    ids1 = inp.topk_ids[:, :1].copy()
+    lay = oracle.layout(ids1, w.E, w.R)
+    y = oracle.dispatch_bf16(inp.tokens, lay.dst_row)
+    w1 = inp.topk_weights[:, :1].copy()
+    assert np.array_equal(oracle.combine_rank_partial(y, w1, ids1, lay.dst_row, w.E, w.R),
+                          oracle.combine(y, w1, lay.dst_row))
+
+
+def test_rank_partial_accuracy_cost(oracle):
+    """The sender-side scheme is within its extra rounding bound of the exact
+    sum, and it does differ from the receiver-side result on real routing."""
+    w = wl.get("decode_dsv3")
+    inp = wl.make_inputs(w, T=64)
+    lay = oracle.layout(inp.topk_ids, w.E, w.R)
+    y = wl.to_bf16_bits(f32(oracle.dispatch_bf16(inp.tokens, lay.dst_row)) *
+                        inp.expert_scale[np.searchsorted(lay.expert_offsets[1:], np.arange(64 * w.K), side="right")][:, None])
+    part = f32(oracle.combine_rank_partial(y, inp.topk_weights, inp.topk_ids, lay.dst_row, w.E, w.R)).astype(np.float64)
+    recv = f32(oracle.combine(y, inp.topk_weights, lay.dst_row)).astype(np.float64)
+    yd = f32(y).astype(np.float64)
+    terms = inp.topk_weights.astype(np.float64)[:, :, None] * yd[lay.dst_row]
+    exact = terms.sum(axis=1)
+    mag = np.abs(terms).sum(axis=1)
+    # each of <= K partials rounds to bf16 (2^-9 relative), plus the final rounding
+    assert np.all(np.abs(part - exact) <= mag * (w.K + 1) * 2.0 ** -8 + 1e-30)
+    assert np.count_nonzero(part != recv) > 0
+
+
+def test_rank_partial_order_sensitive(oracle):
+    """Terms 2^30, -2^30, 1 (2^30 + 1 rounds to 2^30 in fp32): in the defined
+    orders the sum is exactly 1, any other order gives 0."""
+    big = 2.0 ** 30
+    # ranks in ascending order: experts 0, 2, 4 on ranks 0, 1, 2 (E=6, R=3)
+    ids_a = np.array([[4, 2, 0]], np.int32)
+    lay_a = oracle.layout(ids_a, 6, 3)
+    y_a = np.zeros((3, 8), np.float32)
+    y_a[lay_a.dst_row[0, 2]] = big         # expert 0, rank 0
+    y_a[lay_a.dst_row[0, 1]] = -big        # expert 2, rank 1
+    y_a[lay_a.dst_row[0, 0]] = 1.0         # expert 4, rank 2
+    w = np.ones((1, 3), np.float32)
+    got_a = oracle.combine_rank_partial(wl.to_bf16_bits(y_a), w, ids_a, lay_a.dst_row, 6, 3)
+    assert np.all(f32(got_a) == 1.0)
+    # k order inside one rank: experts 0, 1, 2 all on rank 0 (E=6, R=2)
+    ids_b = np.array([[0, 1, 2]], np.int32)
+    lay_b = oracle.layout(ids_b, 6, 2)
+    y_b = np.zeros((3, 8), np.float32)
+    for k, v in enumerate((big, -big, 1.0)):
+        y_b[lay_b.dst_row[0, k]] = v
+    got_b = oracle.combine_rank_partial(wl.to_bf16_bits(y_b), w, ids_b, lay_b.dst_row, 6, 2)
+    assert np.all(f32(got_b) == 1.0)
+    for yb, ids, lay, R in ((y_a, ids_a, lay_a, 3), (y_b, ids_b, lay_b, 2)):
+        yb16 = wl.to_bf16_bits(yb)
+        assert np.array_equal(oracle.combine_rank_partial(yb16, w, ids, lay.dst_row, 6, R),
+                              exact_rank_partial(yb16, w, ids, lay.dst_row, 6, R))
