@@ -84,6 +84,10 @@ def _load():
             lib.oracle_combine_fp8.restype = None
             lib.oracle_combine_rank_partial.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, P]
             lib.oracle_combine_rank_partial.restype = None
+            lib.oracle_dispatch_send.argtypes = [P, P, P, i32, i32, i32, i32, i32, P, P, P, P]
+            lib.oracle_dispatch_send.restype = ctypes.c_uint32
+            lib.oracle_dispatch_recv.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, P, P]
+            lib.oracle_dispatch_recv.restype = None
             _lib = lib
     return _lib
 
@@ -236,3 +240,46 @@ def combine_rank_partial(y_bits: np.ndarray, topk_weights: np.ndarray,
     _load().oracle_combine_rank_partial(_ptr(y), _ptr(w), _ptr(ids), _ptr(d), T, H, K,
                                         E, R, _ptr(out))
     return out
+
+
+def _rows_u8(a):
+    a = np.ascontiguousarray(a)
+    return a.reshape(a.shape[0], -1).view(np.uint8)
+
+
+def dispatch_send(packed: np.ndarray, scales, rank_offsets: np.ndarray, P: int, C: int):
+    """Split the dispatched rows into per-rank private [R,P,row_bytes] and bulk
+    [R,C,row_bytes] regions (plus scale regions for FP8); returns
+    (priv, priv_scales, bulk, bulk_scales, err)."""
+    rows = np.ascontiguousarray(packed)
+    rb = rows.shape[1] * rows.itemsize
+    u8 = rows.view(np.uint8).reshape(rows.shape[0], rb)
+    sc = None if scales is None else np.ascontiguousarray(scales, np.float32)
+    nb = 0 if sc is None else sc.shape[1]
+    R = rank_offsets.size - 1
+    priv = np.zeros((R, P, rb), np.uint8)
+    bulk = np.zeros((R, C, rb), np.uint8)
+    ps = None if sc is None else np.zeros((R, P, nb), np.float32)
+    bs = None if sc is None else np.zeros((R, C, nb), np.float32)
+    ro = _c(rank_offsets, np.int32)
+    err = _load().oracle_dispatch_send(
+        _ptr(u8), _ptr(sc) if sc is not None else None, _ptr(ro), R, rb, nb, P, C,
+        _ptr(priv), _ptr(ps) if ps is not None else None, _ptr(bulk),
+        _ptr(bs) if bs is not None else None)
+    return priv, ps, bulk, bs, int(err)
+
+
+def dispatch_recv(priv, priv_scales, bulk, bulk_scales, rank_offsets: np.ndarray,
+                  rows: int):
+    """Regions back to slot order: returns (packed_bytes [rows, row_bytes], scales)."""
+    R, P, rb = priv.shape
+    C = bulk.shape[1]
+    nb = 0 if priv_scales is None else priv_scales.shape[2]
+    packed = np.zeros((rows, rb), np.uint8)
+    scales = None if priv_scales is None else np.zeros((rows, nb), np.float32)
+    ro = _c(rank_offsets, np.int32)
+    _load().oracle_dispatch_recv(
+        _ptr(_c(priv, np.uint8)), _ptr(_c(priv_scales, np.float32)) if priv_scales is not None else None,
+        _ptr(_c(bulk, np.uint8)), _ptr(_c(bulk_scales, np.float32)) if bulk_scales is not None else None,
+        _ptr(ro), R, rb, nb, P, C, _ptr(packed), _ptr(scales) if scales is not None else None)
+    return packed, scales

@@ -363,3 +363,78 @@ void oracle_combine_rank_partial(const uint16_t *y, const float *topk_weights,
             out[(int64_t)t * H + j] = oracle_f32_to_bf16(total);
         }
 }
+
+/* ------------------------------------------------------------------------ */
+/* Send and receive regions per destination rank.                           */
+/* ------------------------------------------------------------------------ */
+
+/* "Send/receive buffers": a receiving rank can get at most a bounded number
+ * of tokens; senders write them contiguously once the routing information
+ * (the per-expert counts) is known, and a small private area per sender on
+ * each receiver takes the first tokens early, before the routing is known;
+ * the rest go in one write per peer.  Reading for one sender and R
+ * destinations: rank r's rows, in slot order i = 0 .. n_r - 1
+ * (n_r = rank_offsets[r+1] - rank_offsets[r]), go to its private area for
+ * i < P and to its contiguous bulk area at row i - P otherwise; a bulk row
+ * at or beyond the capacity C is not written and sets error bit 4.  Rows
+ * are the dispatched rows (bf16 copies, or e4m3 codes plus their block
+ * scales), so receive (regions -> slot order) returns exactly the
+ * dispatch output.  priv is [R, P, row_bytes], bulk is [R, C, row_bytes];
+ * the scale arrays (fp8 only) are [R, P, H/128] and [R, C, H/128]. */
+uint32_t oracle_dispatch_send(const uint8_t *packed, const float *scales,
+                              const int32_t *rank_offsets, int32_t R,
+                              int32_t row_bytes, int32_t nb, int32_t P,
+                              int32_t C, uint8_t *priv, float *priv_scales,
+                              uint8_t *bulk, float *bulk_scales)
+{
+    uint32_t err = 0;
+    for (int32_t r = 0; r < R; ++r) {
+        int32_t n_r = rank_offsets[r + 1] - rank_offsets[r];
+        for (int32_t i = 0; i < n_r; ++i) {
+            int64_t src = (int64_t)rank_offsets[r] + i;
+            uint8_t *dst;
+            float *dsc;
+            if (i < P) {
+                dst = priv + ((int64_t)r * P + i) * row_bytes;
+                dsc = priv_scales ? priv_scales + ((int64_t)r * P + i) * nb : 0;
+            } else if (i - P < C) {
+                dst = bulk + ((int64_t)r * C + (i - P)) * row_bytes;
+                dsc = bulk_scales ? bulk_scales + ((int64_t)r * C + (i - P)) * nb : 0;
+            } else {
+                err |= 4u;
+                continue;
+            }
+            memcpy(dst, packed + src * row_bytes, (size_t)row_bytes);
+            if (dsc) memcpy(dsc, scales + src * nb, sizeof(float) * (size_t)nb);
+        }
+    }
+    return err;
+}
+
+/* The receiving side: regions back to slot order (the grouped-GEMM input). */
+void oracle_dispatch_recv(const uint8_t *priv, const float *priv_scales,
+                          const uint8_t *bulk, const float *bulk_scales,
+                          const int32_t *rank_offsets, int32_t R, int32_t row_bytes,
+                          int32_t nb, int32_t P, int32_t C, uint8_t *packed,
+                          float *scales)
+{
+    for (int32_t r = 0; r < R; ++r) {
+        int32_t n_r = rank_offsets[r + 1] - rank_offsets[r];
+        for (int32_t i = 0; i < n_r; ++i) {
+            int64_t dst = (int64_t)rank_offsets[r] + i;
+            const uint8_t *src;
+            const float *ssc;
+            if (i < P) {
+                src = priv + ((int64_t)r * P + i) * row_bytes;
+                ssc = priv_scales ? priv_scales + ((int64_t)r * P + i) * nb : 0;
+            } else if (i - P < C) {
+                src = bulk + ((int64_t)r * C + (i - P)) * row_bytes;
+                ssc = bulk_scales ? bulk_scales + ((int64_t)r * C + (i - P)) * nb : 0;
+            } else {
+                continue;
+            }
+            memcpy(packed + dst * row_bytes, src, (size_t)row_bytes);
+            if (ssc) memcpy(scales + dst * nb, ssc, sizeof(float) * (size_t)nb);
+        }
+    }
+}

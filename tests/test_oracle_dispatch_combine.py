@@ -452,3 +452,51 @@ def test_rank_partial_order_sensitive(oracle):
         yb16 = wl.to_bf16_bits(yb)
         assert np.array_equal(oracle.combine_rank_partial(yb16, w, ids, lay.dst_row, 6, R),
                               exact_rank_partial(yb16, w, ids, lay.dst_row, 6, R))
+
+
+# ------------------------------------------ send / receive regions per rank --
+
+@pytest.mark.parametrize("fp8", [False, True])
+@pytest.mark.parametrize("P", [0, 3, 1000])
+def test_regions_round_trip_and_contents(oracle, fp8, P):
+    """Receive(send(x)) is the dispatch output, and every region row is the
+    matching slice of it: private rows first, then the bulk rows."""
+    w = wl.get("decode_dsv3")
+    inp = wl.make_inputs(w, T=40)
+    lay = oracle.layout(inp.topk_ids, w.E, w.R)
+    if fp8:
+        packed, scales = oracle.dispatch_fp8(inp.tokens, lay.dst_row)
+    else:
+        packed, scales = oracle.dispatch_bf16(inp.tokens, lay.dst_row), None
+    n = np.diff(lay.rank_offsets)
+    C = 40 * min(w.K, w.E // w.R)                  # worst case per region
+    priv, ps, bulk, bs, err = oracle.dispatch_send(packed, scales, lay.rank_offsets, P, C)
+    assert err == 0
+    rows = packed.view(np.uint8).reshape(packed.shape[0], -1)
+    for r in range(w.R):
+        base, nr = lay.rank_offsets[r], n[r]
+        k = min(P, nr)
+        assert np.array_equal(priv[r, :k], rows[base:base + k])
+        assert np.array_equal(bulk[r, :nr - k], rows[base + k:base + nr])
+        if fp8:
+            assert np.array_equal(ps[r, :k], scales[base:base + k])
+            assert np.array_equal(bs[r, :nr - k], scales[base + k:base + nr])
+    back, back_sc = oracle.dispatch_recv(priv, ps, bulk, bs, lay.rank_offsets, packed.shape[0])
+    assert np.array_equal(back, rows)
+    if fp8:
+        assert np.array_equal(back_sc.view(np.uint32), scales.view(np.uint32))
+
+
+def test_regions_overflow(oracle):
+    """A bulk area smaller than a rank's rows keeps what fits, flags bit 4."""
+    ids = np.array([[0, 1], [0, 1], [0, 1], [2, 3]], np.int32)   # rank 0 gets 6 rows
+    lay = oracle.layout(ids, 4, 2)
+    x = wl.to_bf16_bits(np.arange(32, dtype=np.float32).reshape(4, 8))
+    packed = oracle.dispatch_bf16(x, lay.dst_row)
+    priv, _, bulk, _, err = oracle.dispatch_send(packed, None, lay.rank_offsets, 1, 3)
+    assert err == 4
+    rows = packed.view(np.uint8).reshape(8, -1)
+    assert np.array_equal(priv[0, 0], rows[0]) and np.array_equal(bulk[0], rows[1:4])
+    back, _ = oracle.dispatch_recv(priv, None, bulk, None, lay.rank_offsets, 8)
+    assert np.array_equal(back[:4], rows[:4]) and not back[4:6].any()   # dropped rows
+    assert np.array_equal(back[6:], rows[6:])
