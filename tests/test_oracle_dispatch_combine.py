@@ -488,15 +488,18 @@ def test_regions_round_trip_and_contents(oracle, fp8, P):
 
 
 def test_regions_overflow(oracle):
-    """A bulk area smaller than a rank's rows keeps what fits, flags bit 4."""
-    ids = np.array([[0, 1], [0, 1], [0, 1], [2, 3]], np.int32)   # rank 0 gets 6 rows
+    """A bulk area smaller than a rank's rows keeps what fits, flags bit 4 and
+    writes nothing past its capacity (rank 1's bulk area stays untouched)."""
+    ids = np.array([[0, 1], [0, 1], [0, 1], [2, 0]], np.int32)   # rank 0: 7 rows, rank 1: 1
     lay = oracle.layout(ids, 4, 2)
-    x = wl.to_bf16_bits(np.arange(32, dtype=np.float32).reshape(4, 8))
+    assert lay.rank_offsets.tolist() == [0, 7, 8]
+    x = wl.to_bf16_bits(np.arange(1, 33, dtype=np.float32).reshape(4, 8))
     packed = oracle.dispatch_bf16(x, lay.dst_row)
     priv, _, bulk, _, err = oracle.dispatch_send(packed, None, lay.rank_offsets, 1, 3)
     assert err == 4
     rows = packed.view(np.uint8).reshape(8, -1)
     assert np.array_equal(priv[0, 0], rows[0]) and np.array_equal(bulk[0], rows[1:4])
+    assert np.array_equal(priv[1, 0], rows[7]) and not bulk[1].any()
     back, _ = oracle.dispatch_recv(priv, None, bulk, None, lay.rank_offsets, 8)
-    assert np.array_equal(back[:4], rows[:4]) and not back[4:6].any()   # dropped rows
-    assert np.array_equal(back[6:], rows[6:])
+    assert np.array_equal(back[:4], rows[:4]) and not back[4:7].any()   # dropped rows
+    assert np.array_equal(back[7], rows[7])
