@@ -59,11 +59,18 @@ def parse_args(argv=None):
                    help="host time spent timing the oracle baseline")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--path", choices=("packed", "regions"), default="packed",
+                   help="regions: dispatch through per-rank send regions (moe_dispatch_send, "
+                        "private area of --private rows, bulk sized to the worst case) and "
+                        "moe_dispatch_recv back to the packed layout")
+    p.add_argument("--private", type=int, default=4, help="private rows per region (--path regions)")
     p.add_argument("--unfused", action="store_true",
                    help="moe_layout + moe_dispatch as two calls instead of moe_layout_dispatch")
-    p.add_argument("--combine", choices=("bf16", "fp8"), default="bf16",
+    p.add_argument("--combine", choices=("bf16", "fp8", "rank_partial"), default="bf16",
                    help="fp8: combine reads the FP8 dispatch output directly "
-                        "(moe_combine_fp8, identity experts); needs --dispatch fp8")
+                        "(moe_combine_fp8, identity experts; needs --dispatch fp8); "
+                        "rank_partial: sender-side per-rank partial sums "
+                        "(moe_combine_rank_partial)")
     return p.parse_args(argv)
 
 
@@ -119,15 +126,27 @@ def algorithmic_bytes(w, dispatch: str):
         disp = 2 * T * H + T * K * H + 4 * T * K * (H // 128) + 4 * T * K
     comb = 2 * T * K * H + 8 * T * K + 2 * T * H
     comb8 = T * K * H + 4 * T * K * (H // 128) + 8 * T * K + 2 * T * H
+    row = (2 * H if dispatch == "bf16" else H + 4 * (H // 128))
+    send = disp + 4 * T * K
+    recv = 2 * T * K * row + 4 * (R + 1)
     return {"layout": layout, "dispatch": disp, "combine": comb, "combine_fp8": comb8,
+            "dispatch_send": send, "dispatch_recv": recv,
+            "combine_rank_partial": comb + 4 * T * K,
             "layout_dispatch": layout + disp - 4 * T * K}
 
 
 def kernel_source_hash(kernel: str) -> str:
-    srcs = {"layout": ["layout.cu"], "dispatch": ["dispatch.cu", "rowops.cuh"],
-            "combine": ["combine.cu"], "combine_fp8": ["combine.cu"],
-            "layout_dispatch": ["layout_dispatch.cu", "rowops.cuh", "layout.cu",
-                                "dispatch.cu"]}[kernel]
+    srcs = {"layout": ["layout.cu", "layout_common.cuh"],
+            "dispatch": ["dispatch.cu", "rowops.cuh"],
+            "combine": ["combine.cu", "combine_common.cuh"],
+            "combine_fp8": ["combine_fp8.cu", "combine_common.cuh"],
+            "combine_rank_partial": ["combine_rank_partial.cu", "combine_common.cuh"],
+            "layout_dispatch": ["layout_dispatch.cu", "layout_common.cuh", "rowops.cuh",
+                                "layout.cu", "dispatch.cu"],
+            "dispatch_send": ["regions.cu", "rowops.cuh"],
+            "dispatch_recv": ["regions.cu"]}.get(kernel)
+    if srcs is None:
+        return None
     h = hashlib.sha256()
     for f in srcs + ["common.cuh"]:
         with open(os.path.join(ROOT, "combine_moe_layout_05_gb300", "csrc", f), "rb") as fh:
@@ -295,7 +314,7 @@ class Driver:
 class BufferSet:
     """Inputs, layout buffers and outputs of one step, all on the device."""
 
-    def __init__(self, w, dispatch, inp, y_host_bits, device):
+    def __init__(self, w, dispatch, inp, y_host_bits, device, private_rows=None):
         import numpy as np
         import torch
         import combine_moe_layout_05_gb300 as moe
@@ -319,12 +338,22 @@ class BufferSet:
         self.y = None if y_host_bits is None else torch.from_numpy(
             y_host_bits.view(np.int16)).to(device).view(torch.bfloat16)
         self.out = torch.empty((T, H), dtype=torch.bfloat16, device=device)
+        self.priv = self.bulk = self.priv_sc = self.bulk_sc = self.region_err = None
+        if private_rows is not None:      # per-rank send regions, worst-case bulk
+            P, C = private_rows, max(0, T * min(K, w.E // w.R) - private_rows)
+            dt = self.packed.dtype
+            self.priv = torch.zeros((w.R, P, H), dtype=dt, device=device)
+            self.bulk = torch.zeros((w.R, C, H), dtype=dt, device=device)
+            if dispatch == "fp8":
+                self.priv_sc = torch.zeros((w.R, P, H // 128), device=device)
+                self.bulk_sc = torch.zeros((w.R, C, H // 128), device=device)
+            self.region_err = torch.zeros(1, dtype=torch.int32, device=device)
 
     def nbytes(self):
-        ts = [self.inputs, self.packed, self.out,
+        ts = [self.inputs, self.packed, self.out, self.priv, self.bulk, self.priv_sc, self.bulk_sc,
               self.layout.src_token, self.layout.dst_row]
-        ts += [t for t in (self.scales, self.y) if t is not None]
-        return sum(t.numel() * t.element_size() for t in ts)
+        ts += [self.scales, self.y]
+        return sum(t.numel() * t.element_size() for t in ts if t is not None)
 
 
 def input_layout(w):
@@ -362,10 +391,19 @@ def expert_outputs(w, dispatch, inp, buf):
     return y.view(torch.int16).cpu().numpy().view("uint16")
 
 
-def step_ops(moe, dispatch, unfused=False, combine="bf16"):
+def step_ops(moe, dispatch, unfused=False, combine="bf16", path="packed"):
     """The calls of one step, as (name, fn(buffer_set)) in launch order."""
     fp8 = dispatch == "fp8"
-    if unfused:
+    if path == "regions":
+        ops = [("layout", lambda b: b.layout.run(b.ids)),
+               ("dispatch_send", lambda b: moe.moe_dispatch_send(
+                   b.tokens, b.ids, b.layout.dst_row, b.layout.rank_offsets, b.layout.E,
+                   b.layout.R, b.priv, b.bulk, b.priv_sc, b.bulk_sc, fp8=fp8,
+                   dev_error=b.region_err)),
+               ("dispatch_recv", lambda b: moe.moe_dispatch_recv(
+                   b.priv, b.bulk, b.layout.rank_offsets, b.layout.T, b.layout.K, b.packed,
+                   b.priv_sc, b.bulk_sc, b.scales, fp8=fp8))]
+    elif unfused:
         ops = [("layout", lambda b: b.layout.run(b.ids)),
                ("dispatch", lambda b: moe.moe_dispatch(b.tokens, b.layout.dst_row,
                                                        b.packed, b.scales, fp8=fp8))]
@@ -375,13 +413,16 @@ def step_ops(moe, dispatch, unfused=False, combine="bf16"):
     if combine == "fp8":
         ops.append(("combine_fp8", lambda b: moe.moe_combine_fp8(
             b.packed, b.scales, b.weights, b.layout.dst_row, b.out)))
+    elif combine == "rank_partial":
+        ops.append(("combine_rank_partial", lambda b: moe.moe_combine_rank_partial(
+            b.y, b.weights, b.ids, b.layout.dst_row, b.layout.E, b.layout.R, b.out)))
     else:
         ops.append(("combine", lambda b: moe.moe_combine(b.y, b.weights, b.layout.dst_row, b.out)))
     return ops
 
 
-def run_step(moe, buf, dispatch, unfused=False, combine="bf16"):
-    for _, fn in step_ops(moe, dispatch, unfused, combine):
+def run_step(moe, buf, dispatch, unfused=False, combine="bf16", path="packed"):
+    for _, fn in step_ops(moe, dispatch, unfused, combine, path):
         fn(buf)
 
 
@@ -410,6 +451,10 @@ def check_parity(w, dispatch, inp, buf, combine="bf16"):
         ok &= np.array_equal(buf.scales.cpu().numpy().view(np.uint32), es.view(np.uint32))
     if combine == "fp8":
         exp_out = oracle.combine_fp8(ec, es, inp.topk_weights, ref.dst_row)
+    elif combine == "rank_partial":
+        y = buf.y.view(torch.int16).cpu().numpy().view(np.uint16)
+        exp_out = oracle.combine_rank_partial(y, inp.topk_weights, inp.topk_ids, ref.dst_row,
+                                              w.E, w.R)
     else:
         y = buf.y.view(torch.int16).cpu().numpy().view(np.uint16)
         exp_out = oracle.combine(y, inp.topk_weights, ref.dst_row)
@@ -432,6 +477,9 @@ def time_oracle(w, dispatch, inp, y_bits, seconds: float, max_tokens=None, combi
             codes, scales = oracle.dispatch_fp8(x, ref.dst_row)
         if combine == "fp8":
             oracle.combine_fp8(codes, scales, wts, ref.dst_row)
+        elif combine == "rank_partial":
+            oracle.combine_rank_partial(y_bits[: T * w.K], wts, inp.topk_ids[:T], ref.dst_row,
+                                        w.E, w.R)
         else:
             oracle.combine(y_bits[: T * w.K], wts, ref.dst_row)
         n += 1
@@ -491,27 +539,27 @@ def run_ours(args):
     inp = wl.make_inputs(w, seed=shard_seed(w.seed, rank))
     if args.combine == "fp8" and dispatch != "fp8":
         raise SystemExit("--combine fp8 needs FP8 dispatch (--dispatch fp8)")
-    ops = step_ops(moe, dispatch, args.unfused, args.combine)
+    ops = step_ops(moe, dispatch, args.unfused, args.combine, args.path)
+    priv_rows = args.private if args.path == "regions" else None
 
     # rotating buffer sets: total >= 3x L2, so every step starts cold in L2
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
-    first = BufferSet(w, dispatch, inp, None, device)
-    ops[0][1](first)
-    if args.unfused:
-        ops[1][1](first)
+    first = BufferSet(w, dispatch, inp, None, device, priv_rows)
+    for _, fn in ops[:-1]:
+        fn(first)
     torch.cuda.synchronize()
-    y_bits = expert_outputs(w, dispatch, inp, first) if args.combine == "bf16" else None
+    y_bits = expert_outputs(w, dispatch, inp, first) if args.combine != "fp8" else None
     per_set = first.nbytes() + (0 if y_bits is None else y_bits.nbytes)
     n_sets = max(2, math.ceil(3 * l2 / per_set))
-    sets = [BufferSet(w, dispatch, inp, y_bits, device) for _ in range(n_sets)]
+    sets = [BufferSet(w, dispatch, inp, y_bits, device, priv_rows) for _ in range(n_sets)]
     del first
     for b in sets:                       # eager pass: attributes, parity data
-        run_step(moe, b, dispatch, args.unfused, args.combine)
+        run_step(moe, b, dispatch, args.unfused, args.combine, args.path)
     torch.cuda.synchronize()
 
     K = args.steps
     G = max(n_sets, (min(args.graph_steps, max(K, 1)) // n_sets) * n_sets)
-    step = lambda b: run_step(moe, b, dispatch, args.unfused, args.combine)
+    step = lambda b: run_step(moe, b, dispatch, args.unfused, args.combine, args.path)
     g = capture(torch, lambda m, sh: [step(sets[j % n_sets]) for j in range(m)], G)
     rem = K % G
     gr = capture(torch, lambda m, sh: [step(sets[j % n_sets]) for j in range(m)], rem) if rem else None
@@ -578,10 +626,12 @@ def run_ours(args):
         "data": "synthetic",
         "config": {"workload": w.name, "T": w.T, "H": w.H, "E": w.E, "R": w.R,
                    "K": w.K, "dispatch": dispatch,
-                   "combine": ("e4m3 + block scales in (identity experts)" if args.combine == "fp8"
-                               else "bf16 in") + ", f32 accumulate",
+                   "combine": {"fp8": "e4m3 + block scales in (identity experts), f32 accumulate",
+                               "rank_partial": "bf16 in, per-rank f32 partials rounded to bf16, "
+                                               "f32 sum over ranks",
+                               "bf16": "bf16 in, f32 accumulate"}[args.combine],
                    "experts": w.experts, "routing": w.routing,
-                   "calls": [n for n, _ in ops],
+                   "calls": [n for n, _ in ops], "path": args.path,
                    "l2": f"{n_sets} rotating buffer sets, {n_sets * per_set / 1e6:.0f} MB "
                          f"> 3x L2 ({l2 / 1e6:.0f} MB); every step cold in L2",
                    "launch": f"CUDA graphs of {G} steps, programmatic dependent launch",
@@ -593,7 +643,7 @@ def run_ours(args):
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "peak_source": peak_src,
                      "traffic": profiled_traffic(dom, w.name, dispatch)},
-        "e2e": e2e, "gpu_launches": launches_per_step(w, dispatch, args.unfused) * K,
+        "e2e": e2e, "gpu_launches": launches_per_step(w, dispatch, args.unfused, args.path) * K,
         "clocks": clocks, "cpu_baseline": cpu, "parity": parity,
     }
     if rank == 0:
@@ -603,10 +653,12 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def launches_per_step(w, dispatch, unfused) -> int:
+def launches_per_step(w, dispatch, unfused, path="packed") -> int:
     """Kernels this library launches per step (mirrors the C ABI's plans)."""
     import combine_moe_layout_05_gb300 as moe
     layout_kernels = 1 if moe.moe_layout_workspace_bytes(w.T, w.K, w.E) == 0 else 3
+    if path == "regions":
+        return layout_kernels + 3
     if unfused:
         return layout_kernels + 2
     return moe.moe_layout_dispatch_kernels(w.T, w.H, w.K, w.E, dispatch == "fp8") + 1
@@ -649,7 +701,7 @@ def run_e2e(args, w, dispatch, inp, sets, n_sets, device, torch, moe, drv):
             comp.wait_event(up_done)
             if j - n_sets in down_done:       # the set's previous output was read
                 comp.wait_event(down_done[j - n_sets])
-            run_step(moe, b, dispatch, args.unfused, args.combine)
+            run_step(moe, b, dispatch, args.unfused, args.combine, args.path)
             comp_done[j] = torch.cuda.Event()
             comp_done[j].record(comp)
             with torch.cuda.stream(down):

@@ -9,7 +9,8 @@ dispatch and combine.
 from ._binding import (MOE_DEV_ERR_DUPLICATE, MOE_DEV_ERR_EXPERT_RANGE,
                        LayoutBuffers, MoeError, declared_functions,
                        library_path, load, moe_combine, moe_combine_fp8,
-                       moe_dispatch,
+                       moe_combine_rank_partial,
+                       moe_dispatch, moe_dispatch_recv, moe_dispatch_send,
                        moe_layout, moe_layout_dispatch,
                        moe_layout_dispatch_kernels, moe_layout_static,
                        moe_layout_workspace_bytes,
@@ -18,8 +19,8 @@ from ._binding import (MOE_DEV_ERR_DUPLICATE, MOE_DEV_ERR_EXPERT_RANGE,
 __all__ = [
     "MOE_DEV_ERR_DUPLICATE", "MOE_DEV_ERR_EXPERT_RANGE", "LayoutBuffers",
     "MoeError", "declared_functions", "library_path", "load", "moe_combine",
-    "moe_combine_fp8",
-    "moe_dispatch", "moe_layout", "moe_layout_dispatch", "moe_layout_dispatch_kernels", "moe_layout_static",
+    "moe_combine_fp8", "moe_combine_rank_partial",
+    "moe_dispatch", "moe_dispatch_recv", "moe_dispatch_send", "moe_layout", "moe_layout_dispatch", "moe_layout_dispatch_kernels", "moe_layout_static",
     "moe_layout_workspace_bytes",
     "moe_status_string",
 ]

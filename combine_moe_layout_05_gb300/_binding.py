@@ -64,6 +64,14 @@ def load(path: str | None = None):
             lib.moe_layout_dispatch_kernels.restype = i32
             lib.moe_combine_fp8.argtypes = [P, P, P, P, i32, i32, i32, P, P]
             lib.moe_combine_fp8.restype = ctypes.c_int
+            lib.moe_combine_rank_partial.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, P, P]
+            lib.moe_combine_rank_partial.restype = ctypes.c_int
+            lib.moe_dispatch_send.argtypes = [P, i32, i32, i32, i32, i32, P, P, P, i32, i32,
+                                              P, P, i32, P, P, P, P]
+            lib.moe_dispatch_send.restype = ctypes.c_int
+            lib.moe_dispatch_recv.argtypes = [P, P, i32, P, P, i32, P, i32, i32, i32, i32,
+                                              i32, P, P, P]
+            lib.moe_dispatch_recv.restype = ctypes.c_int
             lib.moe_layout_static.argtypes = [P, i32, i32, i32, i32, P, P, P, P, P, P, P]
             lib.moe_layout_static.restype = ctypes.c_int
             _lib = lib
@@ -213,6 +221,71 @@ def moe_combine(expert_out, topk_weights, dst_row, out, stream=None) -> None:
     st = load().moe_combine(_ptr(expert_out), _ptr(topk_weights), _ptr(dst_row),
                             T, H, K, _ptr(out), _stream(stream))
     _raise("moe_combine", st)
+
+
+def moe_combine_rank_partial(expert_out, topk_weights, topk_ids, dst_row, E: int,
+                             R: int, out, stream=None) -> None:
+    """Combine with sender-side per-rank partial sums (bf16 partials)."""
+    T, K = topk_weights.shape
+    H = out.shape[1]
+    _check("expert_out", expert_out, torch.bfloat16)
+    _check("topk_weights", topk_weights, torch.float32)
+    _check("topk_ids", topk_ids, torch.int32)
+    _check("dst_row", dst_row, torch.int32)
+    _check("out", out, torch.bfloat16)
+    if dst_row.numel() != T * K or topk_ids.numel() != T * K or out.shape[0] != T \
+            or expert_out.numel() < T * K * H:
+        raise ValueError("moe_combine_rank_partial: argument sizes disagree")
+    st = load().moe_combine_rank_partial(_ptr(expert_out), _ptr(topk_weights), _ptr(topk_ids),
+                                         _ptr(dst_row), T, H, K, E, R, _ptr(out),
+                                         _stream(stream))
+    _raise("moe_combine_rank_partial", st)
+
+
+def moe_dispatch_send(tokens, topk_ids, dst_row, rank_offsets, E: int, R: int,
+                      priv, bulk, priv_scales=None, bulk_scales=None, fp8: bool = False,
+                      dev_error=None, stream=None) -> None:
+    """Dispatch into per-rank regions: priv [R,P,H] for each rank's first P
+    rows, bulk [R,C,H] for the rest (bf16, or e4m3 codes + block scales)."""
+    T, H = tokens.shape
+    K = topk_ids.shape[1]
+    R_, P = priv.shape[0], priv.shape[1]
+    C = bulk.shape[1]
+    if R_ != R or bulk.shape[0] != R:
+        raise ValueError("moe_dispatch_send: region buffers must have R rows of regions")
+    _check("tokens", tokens, torch.bfloat16)
+    for n, t in (("topk_ids", topk_ids), ("dst_row", dst_row), ("rank_offsets", rank_offsets)):
+        _check(n, t, torch.int32)
+    dt = torch.float8_e4m3fn if fp8 else torch.bfloat16
+    _check("priv", priv, dt)
+    _check("bulk", bulk, dt)
+    if fp8:
+        _check("priv_scales", priv_scales, torch.float32)
+        _check("bulk_scales", bulk_scales, torch.float32)
+    st = load().moe_dispatch_send(_ptr(tokens), T, H, K, E, R, _ptr(topk_ids), _ptr(dst_row),
+                                  _ptr(rank_offsets), int(bool(fp8)), P, _ptr(priv),
+                                  _ptr(priv_scales) if fp8 else None, C, _ptr(bulk),
+                                  _ptr(bulk_scales) if fp8 else None, _ptr(dev_error),
+                                  _stream(stream))
+    _raise("moe_dispatch_send", st)
+
+
+def moe_dispatch_recv(priv, bulk, rank_offsets, T: int, K: int, packed,
+                      priv_scales=None, bulk_scales=None, scales=None, fp8: bool = False,
+                      stream=None) -> None:
+    """Region rows back to slot order (the grouped-GEMM input)."""
+    R, P = priv.shape[0], priv.shape[1]
+    C = bulk.shape[1]
+    H = packed.shape[1]
+    _check("rank_offsets", rank_offsets, torch.int32)
+    dt = torch.float8_e4m3fn if fp8 else torch.bfloat16
+    for n, t in (("priv", priv), ("bulk", bulk), ("packed", packed)):
+        _check(n, t, dt)
+    st = load().moe_dispatch_recv(_ptr(priv), _ptr(priv_scales) if fp8 else None, P,
+                                  _ptr(bulk), _ptr(bulk_scales) if fp8 else None, C,
+                                  _ptr(rank_offsets), R, T, H, K, int(bool(fp8)), _ptr(packed),
+                                  _ptr(scales) if fp8 else None, _stream(stream))
+    _raise("moe_dispatch_recv", st)
 
 
 def moe_layout_static(topk_ids, E: int, R: int, expert_counts, expert_offsets,

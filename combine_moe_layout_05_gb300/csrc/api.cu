@@ -126,6 +126,71 @@ moe_status_t moe_combine_fp8(const void *expert_out, const float *expert_scales,
                                                dst_row, T, H, K, out, stream));
 }
 
+moe_status_t moe_combine_rank_partial(const void *expert_out, const float *topk_weights,
+                                      const int32_t *topk_ids, const int32_t *dst_row,
+                                      int32_t T, int32_t H, int32_t K, int32_t E,
+                                      int32_t R, void *out, cudaStream_t stream)
+{
+    moe_status_t s = rows_ok(T, H, K);
+    if (s != MOE_OK) return s;
+    if (E < 1 || E > MOE_MAX_EXPERTS || R < 1 || E % R != 0) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;
+    if (!expert_out || !topk_weights || !topk_ids || !dst_row || !out) return MOE_ERR_INVALID_ARG;
+    if (!aligned(expert_out, 16) || !aligned(out, 16) || !aligned(topk_weights, 4) ||
+        !aligned(topk_ids, 4) || !aligned(dst_row, 4))
+        return MOE_ERR_ALIGNMENT;
+    return cuda_status(moe::launch_combine_rank_partial(expert_out, topk_weights, topk_ids,
+                                                        dst_row, T, H, K, E, R, out, stream));
+}
+
+moe_status_t moe_dispatch_send(const void *tokens, int32_t T, int32_t H, int32_t K,
+                               int32_t E, int32_t R, const int32_t *topk_ids,
+                               const int32_t *dst_row, const int32_t *rank_offsets,
+                               int32_t fp8, int32_t P, void *priv, float *priv_scales,
+                               int32_t C, void *bulk, float *bulk_scales,
+                               uint32_t *dev_error, cudaStream_t stream)
+{
+    moe_status_t s = rows_ok(T, H, K);
+    if (s != MOE_OK) return s;
+    if (E < 1 || E > MOE_MAX_EXPERTS || K > E || R < 1 || E % R != 0 || P < 0 || C < 0)
+        return MOE_ERR_INVALID_ARG;
+    if ((fp8 != 0 && fp8 != 1) || (fp8 && H % 128 != 0)) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;
+    if (!tokens || !topk_ids || !dst_row || !rank_offsets || (P > 0 && !priv) ||
+        (C > 0 && !bulk) || (fp8 && ((P > 0 && !priv_scales) || (C > 0 && !bulk_scales))))
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned(tokens, 16) || !aligned(priv, 16) || !aligned(bulk, 16) ||
+        !aligned(topk_ids, 4) || !aligned(dst_row, 4) || !aligned(rank_offsets, 4) ||
+        !aligned(priv_scales, 4) || !aligned(bulk_scales, 4) || !aligned(dev_error, 4))
+        return MOE_ERR_ALIGNMENT;
+    return cuda_status(moe::launch_dispatch_send(tokens, T, H, K, E, R, topk_ids, dst_row,
+                                                 rank_offsets, fp8, P, priv, priv_scales, C,
+                                                 bulk, bulk_scales, dev_error, stream));
+}
+
+moe_status_t moe_dispatch_recv(const void *priv, const float *priv_scales, int32_t P,
+                               const void *bulk, const float *bulk_scales, int32_t C,
+                               const int32_t *rank_offsets, int32_t R, int32_t T, int32_t H,
+                               int32_t K, int32_t fp8, void *packed, float *scales,
+                               cudaStream_t stream)
+{
+    moe_status_t s = rows_ok(T, H, K);
+    if (s != MOE_OK) return s;
+    if (R < 1 || R > MOE_MAX_EXPERTS || P < 0 || C < 0) return MOE_ERR_INVALID_ARG;
+    if ((fp8 != 0 && fp8 != 1) || (fp8 && H % 128 != 0)) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;
+    if (!rank_offsets || !packed || (P > 0 && !priv) || (C > 0 && !bulk) ||
+        (fp8 && (!scales || (P > 0 && !priv_scales) || (C > 0 && !bulk_scales))))
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned(priv, 16) || !aligned(bulk, 16) || !aligned(packed, 16) ||
+        !aligned(rank_offsets, 4) || !aligned(scales, 4) || !aligned(priv_scales, 4) ||
+        !aligned(bulk_scales, 4))
+        return MOE_ERR_ALIGNMENT;
+    return cuda_status(moe::launch_dispatch_recv(priv, priv_scales, P, bulk, bulk_scales, C,
+                                                 rank_offsets, R, T, H, K, fp8, packed, scales,
+                                                 stream));
+}
+
 moe_status_t moe_layout_dispatch(const int32_t *topk_ids, const void *tokens,
                                  int32_t T, int32_t H, int32_t K, int32_t E,
                                  int32_t R, int32_t fp8, int32_t *expert_counts,

@@ -22,6 +22,22 @@ __device__ __forceinline__ uint4 ld_stream_v4(const void *p)
     return r;
 }
 
+// 8-byte load of read-only data touched once (no L1 allocation).
+__device__ __forceinline__ uint2 ld_stream_v2(const void *p)
+{
+    uint2 r;
+    asm("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];"
+        : "=r"(r.x), "=r"(r.y)
+        : "l"(p));
+    return r;
+}
+
+// 8-byte store.
+__device__ __forceinline__ void st_v2(void *p, const uint2 &v)
+{
+    asm volatile("st.global.v2.u32 [%0], {%1, %2};" :: "l"(p), "r"(v.x), "r"(v.y) : "memory");
+}
+
 // 16-byte store.
 __device__ __forceinline__ void st_v4(void *p, const uint4 &v)
 {

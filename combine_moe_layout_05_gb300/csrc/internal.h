@@ -42,6 +42,21 @@ cudaError_t launch_combine_fp8(const void *codes, const float *scales,
                                const float *topk_weights, const int32_t *dst_row,
                                int T, int H, int K, void *out, cudaStream_t stream);
 
+cudaError_t launch_combine_rank_partial(const void *expert_out, const float *topk_weights,
+                                        const int32_t *topk_ids, const int32_t *dst_row,
+                                        int T, int H, int K, int E, int R, void *out,
+                                        cudaStream_t stream);
+
+cudaError_t launch_dispatch_send(const void *tokens, int T, int H, int K, int E, int R,
+                                 const int32_t *topk_ids, const int32_t *dst_row,
+                                 const int32_t *rank_offsets, int fp8, int P, void *priv,
+                                 float *priv_scales, int C, void *bulk, float *bulk_scales,
+                                 uint32_t *dev_error, cudaStream_t stream);
+cudaError_t launch_dispatch_recv(const void *priv, const float *priv_scales, int P,
+                                 const void *bulk, const float *bulk_scales, int C,
+                                 const int32_t *rank_offsets, int R, int T, int H, int K,
+                                 int fp8, void *packed, float *scales, cudaStream_t stream);
+
 // Layout and dispatch together: one fused kernel when
 // layout_dispatch_fused() says the batch is small enough, else the layout
 // kernels followed by the dispatch kernel.

@@ -9,15 +9,16 @@
 // This kernel does both in one launch without any block waiting for another:
 //
 //  * block (t, c) packs slice c of token t's row;
-//  * before that, every block copies all T*K ids into its shared memory
-//    (asynchronous copies, one memory latency) and counts there, for each of
-//    its token's K entries (t, k) with expert e, the valid ids below e (that
-//    is offsets[e]), the entries of e before token t and the earlier k' of
-//    token t with id e; their sum is the slot, the same stable order as
-//    moe_layout.  One pass over the ids with K predicated counters per
-//    thread and one block reduction; no histogram, no scan, no atomics;
-//  * the row slice is loaded before the histogram work, so the HBM latency
-//    of the token row overlaps it;
+//  * before that, every block reads all T*K ids (16-byte loads into
+//    registers) and counts, for each of its token's K entries (t, k) with
+//    expert e, the valid ids below e (that is offsets[e]), the entries of e
+//    before token t and the earlier k' of token t with id e; their sum is
+//    the slot, the same stable order as moe_layout.  One pass over the ids
+//    with the counters packed two to a word, a warp reduction and one
+//    barrier, after which every thread adds the warps' partial sums itself
+//    and holds the slots in registers; no histogram, no scan, no atomics;
+//  * the row slice is requested first, so its HBM latency overlaps the
+//    counting;
 //  * slice 0 of each token writes its dst_row / src_token entries; block b
 //    also counts expert b (count and offset, and the rank offset when b
 //    starts a rank), and block 0 writes the error word.
@@ -37,26 +38,18 @@ constexpr int kThreads = 256;
 constexpr int kMaxEntries = 8192;
 constexpr long long kMaxRedundantEntries = 1ll << 22;
 
-// Sum over the block of N per-thread counters; the totals land in out[0..N)
-// (shared memory) and are visible to every thread on return.
-template <int N>
-__device__ __forceinline__ void block_sum(const int (&v)[N], int32_t (*red)[16],
-                                          int32_t *out)
+// Adds, for the 8 targets tg[] (and the block's expert role), this entry's
+// contributions to the packed 16-bit counters (two per 32-bit word; every
+// count is at most T*K <= kMaxEntries < 2^16, so halves never carry).
+__device__ __forceinline__ void count_entry(int x, int i, int mine, int E, int role,
+                                            const int (&tg)[8], uint32_t (&v)[5])
 {
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    if ((unsigned)x >= (unsigned)E) return;
+    const bool before = i < mine;
 #pragma unroll
-    for (int j = 0; j < N; ++j) {
-        const int s = __reduce_add_sync(kFullMask, v[j]);
-        if (lane == 0) red[w][j] = s;
-    }
-    __syncthreads();
-    if (threadIdx.x < N) {
-        int s = 0;
-#pragma unroll
-        for (int q = 0; q < kThreads / 32; ++q) s += red[q][threadIdx.x];
-        out[threadIdx.x] = s;
-    }
-    __syncthreads();
+    for (int j = 0; j < 8; ++j)
+        v[j >> 1] += (uint32_t)((x < tg[j]) | ((x == tg[j]) & before)) << (16 * (j & 1));
+    v[4] += (uint32_t)(x < role) | ((uint32_t)(x == role) << 16);
 }
 
 template <int KT, bool kFp8>
@@ -69,13 +62,11 @@ layout_dispatch_kernel(const int32_t *__restrict__ ids, const uint4 *__restrict_
                        uint32_t *__restrict__ dev_error, uint8_t *__restrict__ packed,
                        float *__restrict__ scales)
 {
-    extern __shared__ __align__(16) int32_t ids_s[];   // [T*K]
-    __shared__ int32_t red[kThreads / 32][16];
-    __shared__ int32_t sums[16];
-    __shared__ int32_t slots[MOE_MAX_TOPK];
+    __shared__ uint32_t red[kThreads / 32][8];
+    __shared__ int32_t slots_s[MOE_MAX_TOPK];
     __shared__ uint32_t s_err;
 
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     const int nb = gridDim.x, b = blockIdx.x;
     const int t = b / chunks, c = b - (b / chunks) * chunks;
     const int k_count = KT > 0 ? KT : K;
@@ -85,12 +76,14 @@ layout_dispatch_kernel(const int32_t *__restrict__ ids, const uint4 *__restrict_
     const int u0 = c * upc, u1 = min(units, u0 + upc);
     const size_t vrow = (size_t)(H >> 3);
     const int epr = E / R;
+    constexpr bool kRegSlots = KT > 0 && KT <= 8;   // slots live in registers
+    const bool vec_ids = ((reinterpret_cast<uintptr_t>(ids) & 15) == 0) && (n & 3) == 0;
 
     if (tid == 0) s_err = 0;
     pdl_wait();
     pdl_trigger();
 
-    // the first piece of this thread's share of the row, loaded early
+    // this thread's first piece of the row; it arrives while slots are counted
     uint4 a = make_uint4(0, 0, 0, 0), bv = make_uint4(0, 0, 0, 0);
     {
         const int u = u0 + tid;
@@ -103,86 +96,72 @@ layout_dispatch_kernel(const int32_t *__restrict__ ids, const uint4 *__restrict_
             }
         }
     }
-    stage_i32(ids_s, ids, n);
-    cp_async_wait_all();
-    __syncthreads();
 
     // Slots of this token's entries, 8 at a time:
     //   slot(t,k) = #{valid ids < e} + #{entries before token t with id e}
     //             + #{k' < k of token t with id e},  e = ids[t,k].
-    // The first pass also gives block b the count and offset of expert b
-    // (offsets[e] = #{valid ids < e}), so these outputs are spread over the
-    // grid; experts beyond the grid take further passes below.
+    // Each thread counts its share of the ids straight from global memory
+    // (16-byte loads), each warp reduces its packed counters, and after one
+    // barrier every thread adds up the warps' partial sums itself, so the
+    // whole block holds the slots without further synchronisation.  The same
+    // pass gives block b the count and offset of expert b
+    // (offsets[e] = #{valid ids < e}), spreading those outputs over the grid.
+    int sl[8];
     for (int k0 = 0; k0 < k_count; k0 += 8) {
-        int tg[8], v[10];
+        int tg[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) tg[j] = k0 + j < k_count ? __ldg(ids + mine + k0 + j) : -1;
+        const int role = (k0 == 0 && b <= E) ? b : -1;
+        uint32_t v[5] = {0, 0, 0, 0, 0};
+        if (vec_ids) {
+            for (int i = 4 * tid; i < n; i += 4 * kThreads) {
+                const int4 q = __ldg(reinterpret_cast<const int4 *>(ids + i));
+                count_entry(q.x, i, mine, E, role, tg, v);
+                count_entry(q.y, i + 1, mine, E, role, tg, v);
+                count_entry(q.z, i + 2, mine, E, role, tg, v);
+                count_entry(q.w, i + 3, mine, E, role, tg, v);
+            }
+        } else {
+            for (int i = tid; i < n; i += kThreads) count_entry(__ldg(ids + i), i, mine, E, role, tg, v);
+        }
+#pragma unroll
+        for (int j = 0; j < 5; ++j) {
+            const uint32_t sum = __reduce_add_sync(kFullMask, v[j]);
+            if (lane == 0) red[w][j] = sum;
+        }
+        __syncthreads();
+        uint32_t tot[5] = {0, 0, 0, 0, 0};
+#pragma unroll
+        for (int q = 0; q < kThreads / 32; ++q)
+#pragma unroll
+            for (int j = 0; j < 5; ++j) tot[j] += red[q][j];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-            tg[j] = k0 + j < k_count ? ids_s[mine + k0 + j] : -1;
-            v[j] = 0;
-        }
-        const int role = (k0 == 0 && b <= E) ? b : -1;
-        v[8] = v[9] = 0;
-        for (int i = tid; i < n; i += kThreads) {
-            const int x = ids_s[i];
-            if ((unsigned)x >= (unsigned)E) continue;
-            const bool before = i < mine;
+            int dup = 0;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) v[j] += (x < tg[j]) | ((x == tg[j]) & before);
-            v[8] += x < role;
-            v[9] += x == role;
+            for (int x = 0; x < j; ++x) dup += tg[x] == tg[j];
+            for (int x = 0; x < k0; ++x) dup += __ldg(ids + mine + x) == tg[j];
+            const int below = (int)((tot[j >> 1] >> (16 * (j & 1))) & 0xffffu);
+            sl[j] = (unsigned)tg[j] < (unsigned)E ? below + dup : -1;
         }
-        block_sum<10>(v, red, sums);
         if (tid < 8 && k0 + tid < k_count) {
-            const int e = ids_s[mine + k0 + tid];
-            int slot = -1;
-            if ((unsigned)e < (unsigned)E) {
-                int dup = 0;
-                for (int x = 0; x < k0 + tid; ++x) dup += ids_s[mine + x] == e;
-                slot = sums[tid] + dup;
-            }
-            slots[k0 + tid] = slot;
+            int mine_slot = sl[0];
+#pragma unroll
+            for (int j = 1; j < 8; ++j)
+                if (tid == j) mine_slot = sl[j];
+            if (!kRegSlots) slots_s[k0 + tid] = mine_slot;
             if (c == 0) {
-                dst_row[mine + k0 + tid] = slot;
-                if (slot >= 0) src_token[slot] = t;
+                dst_row[mine + k0 + tid] = mine_slot;
+                if (mine_slot >= 0) src_token[mine_slot] = t;
             }
         }
         if (role >= 0 && tid == 0) {
-            offsets[role] = sums[8];
-            if (role < E) counts[role] = sums[9];
-            if (role % epr == 0) rank_offsets[role / epr] = sums[8];
+            const int lt = (int)(tot[4] & 0xffffu), eq = (int)(tot[4] >> 16);
+            offsets[role] = lt;
+            if (role < E) counts[role] = eq;
+            if (role % epr == 0) rank_offsets[role / epr] = lt;
         }
-        __syncthreads();    // sums is reused by the next pass
-    }
-    // experts not covered by the first pass (grids smaller than E + 1)
-    for (int r0 = b + nb; r0 <= E; r0 += 8 * nb) {
-        int v[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) v[j] = 0;
-        for (int i = tid; i < n; i += kThreads) {
-            const int x = ids_s[i];
-            if ((unsigned)x >= (unsigned)E) continue;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                v[2 * j] += x < r0 + j * nb;
-                v[2 * j + 1] += x == r0 + j * nb;
-            }
-        }
-        block_sum<16>(v, red, sums);
-        if (tid < 8) {
-            const int e = r0 + tid * nb;
-            if (e <= E) {
-                offsets[e] = sums[2 * tid];
-                if (e < E) counts[e] = sums[2 * tid + 1];
-                if (e % epr == 0) rank_offsets[e / epr] = sums[2 * tid];
-            }
-        }
-        __syncthreads();
-    }
-    if (b == 0) {
-        const uint32_t err = token_errors(ids_s, T, k_count, E);
-        if (err) atomicOr(&s_err, err);
-        __syncthreads();
-        if (tid == 0 && dev_error) *dev_error = s_err;
+        if (!kRegSlots) __syncthreads();   // red is reused; slots_s complete
     }
 
     const int rows = n;
@@ -197,6 +176,7 @@ layout_dispatch_kernel(const int32_t *__restrict__ ids, const uint4 *__restrict_
                 a = ld_stream_v4(tokens + (size_t)t * vrow + u);
             }
         }
+        const int32_t *slots = kRegSlots ? sl : slots_s;
         if (kFp8) {
             const Fp8Piece p = quantize16(a, bv);   // every lane takes part
             if (active)
@@ -204,6 +184,48 @@ layout_dispatch_kernel(const int32_t *__restrict__ ids, const uint4 *__restrict_
         } else if (active) {
             store_to_slots<KT>(slots, k_count, rows, packed, vrow * 16, (size_t)u * 16, a);
         }
+    }
+
+    // experts not covered by the first pass (grids smaller than E + 1), in
+    // groups of 8: plain 32-bit counters here, these passes are rare
+    if (kRegSlots) __syncthreads();        // red is reused below
+    for (int r0 = b + nb; r0 <= E; r0 += 4 * nb) {
+        uint32_t v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        for (int i = tid; i < n; i += kThreads) {
+            const int x = __ldg(ids + i);
+            if ((unsigned)x >= (unsigned)E) continue;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                v[2 * j] += x < r0 + j * nb;
+                v[2 * j + 1] += x == r0 + j * nb;
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const uint32_t sum = __reduce_add_sync(kFullMask, v[j]);
+            if (lane == 0) red[w][j] = sum;
+        }
+        __syncthreads();
+        if (tid < 4) {
+            const int e = r0 + tid * nb;
+            int lt = 0, eq = 0;
+            for (int q = 0; q < kThreads / 32; ++q) {
+                lt += red[q][2 * tid];
+                eq += red[q][2 * tid + 1];
+            }
+            if (e <= E) {
+                offsets[e] = lt;
+                if (e < E) counts[e] = eq;
+                if (e % epr == 0) rank_offsets[e / epr] = lt;
+            }
+        }
+        __syncthreads();
+    }
+    if (b == 0) {
+        const uint32_t err = token_errors(ids, T, k_count, E);
+        if (err) atomicOr(&s_err, err);
+        __syncthreads();
+        if (tid == 0 && dev_error) *dev_error = s_err;
     }
 }
 
@@ -233,9 +255,8 @@ cudaError_t run_fused(const FusedPlan &p, const int32_t *ids, const void *tokens
                       int32_t *dst_row, uint32_t *dev_error, void *packed,
                       float *scales, cudaStream_t s)
 {
-    const size_t smem = sizeof(int32_t) * (size_t)T * K;
     return launch_pdl(layout_dispatch_kernel<KT, kFp8>, dim3(T * p.chunks), dim3(kThreads),
-                      smem, s, ids, static_cast<const uint4 *>(tokens), T, H, K, E, R,
+                      0, s, ids, static_cast<const uint4 *>(tokens), T, H, K, E, R,
                       p.chunks, p.upc, counts, offsets, rank_offsets, src_token,
                       dst_row, dev_error, static_cast<uint8_t *>(packed), scales);
 }

@@ -16,7 +16,8 @@
  *    allocates and owns every buffer; the library allocates nothing and
  *    never synchronises, and apart from moe_layout_static's scratch array
  *    (described with that call) it keeps no state between calls.
- *  - moe_layout, moe_dispatch, moe_combine, moe_combine_fp8 and
+ *  - moe_layout, moe_dispatch, moe_combine, moe_combine_fp8,
+ *    moe_combine_rank_partial, moe_dispatch_send, moe_dispatch_recv and
  *    moe_layout_dispatch are asynchronous on `stream` (0 = legacy default
  *    stream) and may be captured into a CUDA graph.
  *  - Arguments are checked on the host before anything is enqueued.  A
@@ -60,6 +61,8 @@ typedef enum moe_status {
  * stream has reached that point). */
 #define MOE_DEV_ERR_EXPERT_RANGE 1u  /* some topk_ids entry is outside [0, E)   */
 #define MOE_DEV_ERR_DUPLICATE    2u  /* some token lists one expert twice       */
+#define MOE_DEV_ERR_REGION_OVERFLOW 4u /* moe_dispatch_send: a rank's rows exceed
+                                          its private + bulk capacity          */
 
 /* Limits of this implementation. */
 #define MOE_MAX_EXPERTS 1024
@@ -199,6 +202,70 @@ MOE_API moe_status_t moe_combine_fp8(const void *expert_out, const float *expert
                                      const float *topk_weights, const int32_t *dst_row,
                                      int32_t T, int32_t H, int32_t K, void *out,
                                      cudaStream_t stream);
+
+/*
+ * moe_combine_rank_partial -- combine with sender-side partial sums.
+ *
+ * The page accumulates only on the receiving side and contrasts this with
+ * DeepEP, which sums in the sender to cut the bytes transferred, at some cost
+ * in accuracy ("Evaluation").  This call computes that scheme on the same
+ * data: each token's entries are grouped by the rank r = e / (E/R) hosting
+ * their expert; each group is summed as the fp32 FMA chain in k order from
+ * +0 and rounded to bf16 (the transfer format); the receiver adds the
+ * groups' values as fp32 in ascending rank order from +0 and rounds to bf16.
+ * With R == 1 or K == 1 it equals moe_combine.
+ *
+ * expert_out [T*K,H] bf16 (16-byte aligned), topk_weights [T,K] fp32,
+ * topk_ids [T,K] int32 (the layout's input), dst_row [T,K] int32,
+ * out [T,H] bf16 (16-byte aligned).  1 <= E <= MOE_MAX_EXPERTS, E % R == 0,
+ * H % 8 == 0.  Entries whose expert id or dst_row is invalid are skipped.
+ */
+MOE_API moe_status_t moe_combine_rank_partial(const void *expert_out,
+                                              const float *topk_weights,
+                                              const int32_t *topk_ids,
+                                              const int32_t *dst_row, int32_t T,
+                                              int32_t H, int32_t K, int32_t E, int32_t R,
+                                              void *out, cudaStream_t stream);
+
+/*
+ * moe_dispatch_send / moe_dispatch_recv -- dispatch through per-destination
+ * send regions, then back into the grouped-GEMM input.
+ *
+ * The page's send-buffer design ("Send/receive buffers"): senders lay their
+ * writes out contiguously once the per-expert counts are known; a small
+ * private area per sender on each receiver takes the first tokens before
+ * that, and the rest travel in one write per peer.  With one sender and R
+ * destination ranks (rank r hosts experts r*E/R .. (r+1)*E/R - 1), rank r's
+ * rows in slot order i = 0 .. n_r - 1 (n_r = rank_offsets[r+1] -
+ * rank_offsets[r], from moe_layout) are written to
+ *   priv[r, i]      for i < P          (the private area), or
+ *   bulk[r, i - P]  for P <= i < P + C (the contiguous area),
+ * and rows at i >= P + C are not written.  Rows are what moe_dispatch writes:
+ * bf16 copies (fp8 == 0) or e4m3 codes with their 1x128 block scales
+ * (fp8 == 1).  A region of T * min(K, E/R) rows can never overflow.
+ * moe_dispatch_recv puts every region row back at its slot of `packed`
+ * (and `scales`), so send + recv gives exactly the moe_dispatch output.
+ *
+ * priv   [R, P, row] and bulk [R, C, row], row = H bf16 or H e4m3 bytes;
+ *        16-byte aligned.  priv_scales [R, P, H/128], bulk_scales [R, C, H/128]
+ *        fp32 (fp8 == 1 only).  P >= 0, C >= 0.
+ * topk_ids, dst_row [T, K] int32 and rank_offsets [R+1] int32 from moe_layout.
+ * dev_error (send; may be NULL) is overwritten with
+ *        MOE_DEV_ERR_REGION_OVERFLOW when some n_r exceeds P + C, else 0.
+ * H % 8 == 0 (H % 128 == 0 for fp8), E % R == 0.  T == 0 is a no-op.
+ */
+MOE_API moe_status_t moe_dispatch_send(const void *tokens, int32_t T, int32_t H, int32_t K,
+                                       int32_t E, int32_t R, const int32_t *topk_ids,
+                                       const int32_t *dst_row, const int32_t *rank_offsets,
+                                       int32_t fp8, int32_t P, void *priv, float *priv_scales,
+                                       int32_t C, void *bulk, float *bulk_scales,
+                                       uint32_t *dev_error, cudaStream_t stream);
+
+MOE_API moe_status_t moe_dispatch_recv(const void *priv, const float *priv_scales, int32_t P,
+                                       const void *bulk, const float *bulk_scales, int32_t C,
+                                       const int32_t *rank_offsets, int32_t R, int32_t T,
+                                       int32_t H, int32_t K, int32_t fp8, void *packed,
+                                       float *scales, cudaStream_t stream);
 
 /*
  * moe_layout_dispatch -- moe_layout followed by moe_dispatch, as one call.

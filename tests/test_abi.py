@@ -141,3 +141,16 @@ def test_combine_fp8_host_checks(lib):
     assert c(*args(s=FAKE + 2)) == 2
     assert c(*args(o=FAKE + 4)) == 2
     assert c(None, None, None, None, 0, 256, 2, None, None) == 0   # T == 0: no-op
+
+
+def test_combine_rank_partial_host_checks(lib):
+    c = lib.moe_combine_rank_partial
+    args = lambda **kw: [P(kw.get("y", FAKE)), P(FAKE), P(kw.get("ids", FAKE)), P(FAKE),
+                         kw.get("T", 4), kw.get("H", 64), kw.get("K", 2), kw.get("E", 8),
+                         kw.get("R", 2), P(kw.get("o", FAKE)), None]
+    assert c(*args(R=3)) == 1                    # E % R
+    assert c(*args(E=2000, R=1)) == 1            # E > MOE_MAX_EXPERTS
+    assert c(*args(H=12)) == 1
+    assert c(*args(y=FAKE + 8)) == 2
+    assert c(*args(ids=FAKE + 2)) == 2
+    assert c(None, None, None, None, 0, 64, 2, 8, 2, None, None) == 0
