@@ -350,10 +350,17 @@ class BufferSet:
             self.region_err = torch.zeros(1, dtype=torch.int32, device=device)
 
     def nbytes(self):
-        ts = [self.inputs, self.packed, self.out, self.priv, self.bulk, self.priv_sc, self.bulk_sc,
+        """Bytes a step touches in this set (region buffers count only the
+        rows a step fills: T*K rows, whatever their worst-case capacity)."""
+        ts = [self.inputs, self.packed, self.out,
               self.layout.src_token, self.layout.dst_row]
         ts += [self.scales, self.y]
-        return sum(t.numel() * t.element_size() for t in ts if t is not None)
+        touched = sum(t.numel() * t.element_size() for t in ts if t is not None)
+        if self.priv is not None:     # the filled region rows equal the packed rows
+            touched += self.packed.numel() * self.packed.element_size()
+            if self.scales is not None:
+                touched += self.scales.numel() * self.scales.element_size()
+        return touched
 
 
 def input_layout(w):
@@ -656,7 +663,7 @@ def run_ours(args):
 def launches_per_step(w, dispatch, unfused, path="packed") -> int:
     """Kernels this library launches per step (mirrors the C ABI's plans)."""
     import combine_moe_layout_05_gb300 as moe
-    layout_kernels = 1 if moe.moe_layout_workspace_bytes(w.T, w.K, w.E) == 0 else 3
+    layout_kernels = 1 if moe.moe_layout_workspace_bytes(w.T, w.K, w.E) == 0 else 2
     if path == "regions":
         return layout_kernels + 3
     if unfused:

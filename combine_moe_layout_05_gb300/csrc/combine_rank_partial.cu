@@ -16,93 +16,90 @@
 namespace moe {
 namespace {
 
-__device__ __forceinline__ void fma4(float acc[4], float w, const uint2 &y)
-{
-    acc[0] = __fmaf_rn(w, bf16_lo(y.x), acc[0]);
-    acc[1] = __fmaf_rn(w, bf16_hi(y.x), acc[1]);
-    acc[2] = __fmaf_rn(w, bf16_lo(y.y), acc[2]);
-    acc[3] = __fmaf_rn(w, bf16_hi(y.y), acc[3]);
-}
-
-// A thread owns 4 hidden values (8 bytes): the per-rank pass keeps all K
-// gathered pieces, one partial and one total live, which fits the register
-// budget of a fully occupied SM.  KT > 0: every gather is issued before any
-// arithmetic; a runtime K loads inside the rank loop.
+// One thread per block orders the token's valid entries by (rank, k) in
+// shared memory -- slot, weight, and a bit marking the last entry of each
+// rank's group -- so every thread then gathers its 8 values per entry in that
+// order and makes a single pass: fused multiply-adds into the group's
+// partial, and at each group's end the partial rounded to bf16 is added into
+// the fp32 total.  KT > 0: all gathers are issued before any arithmetic.
 template <int KT>
 __global__ void __launch_bounds__(256)
-combine_rank_partial_kernel(const uint2 *__restrict__ y, const float *__restrict__ weights,
+combine_rank_partial_kernel(const uint4 *__restrict__ y, const float *__restrict__ weights,
                             const int32_t *__restrict__ ids, const int32_t *__restrict__ dst_row,
-                            int K, int vpr, int rows, int E, int epr, uint2 *__restrict__ out)
+                            int K, int vpr, int rows, int E, int epr, uint4 *__restrict__ out)
 {
+    __shared__ int32_t s_row[MOE_MAX_TOPK];
+    __shared__ float s_w[MOE_MAX_TOPK];
+    __shared__ uint32_t s_last;
+    __shared__ int32_t s_n;
     pdl_wait();
     pdl_trigger();
     const int t = blockIdx.x;
     const int v = blockIdx.y * blockDim.x + threadIdx.x;
-    if (v >= vpr) return;
     const int k_count = KT > 0 ? KT : K;
-    const int32_t *d = dst_row + (size_t)t * k_count;
-    const int32_t *ex = ids + (size_t)t * k_count;
-    const float *wt = weights + (size_t)t * k_count;
-
-    // rank of each entry (-1 when its expert or slot is invalid)
-    auto rank_of = [&](int k, int &r) {
-        r = __ldg(d + k);
-        const int e = __ldg(ex + k);
-        const bool ok = (unsigned)r < (unsigned)rows && (unsigned)e < (unsigned)E;
-        return ok ? e / epr : -1;
-    };
-    float total[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    auto flush = [&](const float part[4]) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            total[j] = __fadd_rn(total[j], __bfloat162float(__float2bfloat16_rn(part[j])));
-    };
-
-    if constexpr (KT > 0) {
-        int rk[KT], row[KT];
-        float wk[KT];
-        uint2 val[KT];
-#pragma unroll
-        for (int k = 0; k < KT; ++k) {
-            rk[k] = rank_of(k, row[k]);
-            wk[k] = __ldg(wt + k);
-            val[k] = rk[k] >= 0 ? ld_stream_v2(y + (size_t)row[k] * vpr + v) : make_uint2(0, 0);
+    if (threadIdx.x == 0) {
+        int key[MOE_MAX_TOPK];
+        int n = 0;
+        for (int k = 0; k < k_count; ++k) {
+            const int r = __ldg(dst_row + (size_t)t * k_count + k);
+            const int e = __ldg(ids + (size_t)t * k_count + k);
+            if ((unsigned)r < (unsigned)rows && (unsigned)e < (unsigned)E)
+                key[n++] = ((e / epr) << 5) | k;          // rank major, then k
         }
-        int prev = -1;
-        for (;;) {
-            int cur = 0x7fffffff;
-#pragma unroll
-            for (int k = 0; k < KT; ++k)
-                if (rk[k] > prev && rk[k] < cur) cur = rk[k];
-            if (cur == 0x7fffffff) break;
-            float part[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-            for (int k = 0; k < KT; ++k)
-                if (rk[k] == cur) fma4(part, wk[k], val[k]);
-            flush(part);
-            prev = cur;
-        }
-    } else {
-        int prev = -1;
-        for (;;) {
-            int cur = 0x7fffffff, row;
-            for (int k = 0; k < k_count; ++k) {
-                const int r = rank_of(k, row);
-                if (r > prev && r < cur) cur = r;
+        for (int i = 1; i < n; ++i) {                     // insertion sort, n <= 32
+            const int x = key[i];
+            int j = i - 1;
+            while (j >= 0 && key[j] > x) {
+                key[j + 1] = key[j];
+                --j;
             }
-            if (cur == 0x7fffffff) break;
-            float part[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-            for (int k = 0; k < k_count; ++k)
-                if (rank_of(k, row) == cur)
-                    fma4(part, __ldg(wt + k), ld_stream_v2(y + (size_t)row * vpr + v));
-            flush(part);
-            prev = cur;
+            key[j + 1] = x;
         }
+        uint32_t last = 0;
+        for (int i = 0; i < n; ++i) {
+            const int k = key[i] & 31;
+            s_row[i] = __ldg(dst_row + (size_t)t * k_count + k);
+            s_w[i] = __ldg(weights + (size_t)t * k_count + k);
+            if (i == n - 1 || (key[i] >> 5) != (key[i + 1] >> 5)) last |= 1u << i;
+        }
+        s_last = last;
+        s_n = n;
     }
-    uint2 o;
+    __syncthreads();
+    if (v >= vpr) return;
+    const int n = s_n;
+    const uint32_t last = s_last;
+
+    float total[8], part[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) total[j] = part[j] = 0.0f;
+    auto step = [&](int i, const uint4 &val) {
+        fma8(part, s_w[i], val);
+        if ((last >> i) & 1u) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                total[j] = __fadd_rn(total[j], __bfloat162float(__float2bfloat16_rn(part[j])));
+                part[j] = 0.0f;
+            }
+        }
+    };
+    constexpr int B = KT > 0 ? KT : kBatch;
+    for (int i0 = 0; i0 < n; i0 += B) {
+        uint4 val[B];
+#pragma unroll
+        for (int i = 0; i < B; ++i)
+            val[i] = i0 + i < n ? ld_stream_v4(y + (size_t)s_row[i0 + i] * vpr + v)
+                                : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int i = 0; i < B; ++i)
+            if (i0 + i < n) step(i0 + i, val[i]);
+    }
+    uint4 o;
     o.x = pack_bf16x2_rn(total[0], total[1]);
     o.y = pack_bf16x2_rn(total[2], total[3]);
-    st_v2(out + (size_t)t * vpr + v, o);
+    o.z = pack_bf16x2_rn(total[4], total[5]);
+    o.w = pack_bf16x2_rn(total[6], total[7]);
+    st_v4(out + (size_t)t * vpr + v, o);
 }
 
 template <int KT>
@@ -110,11 +107,11 @@ cudaError_t run_rank_partial(const void *y, const float *w, const int32_t *ids,
                              const int32_t *dst_row, int T, int H, int K, int E, int R,
                              void *out, cudaStream_t s)
 {
-    const int vpr = H / 4;
+    const int vpr = H / 8;
     const int threads = pick_row_block(vpr);
     return launch_pdl(combine_rank_partial_kernel<KT>, dim3(T, ceil_div(vpr, threads)),
-                      dim3(threads), 0, s, static_cast<const uint2 *>(y), w, ids, dst_row,
-                      K, vpr, T * K, E, E / R, static_cast<uint2 *>(out));
+                      dim3(threads), 0, s, static_cast<const uint4 *>(y), w, ids, dst_row,
+                      K, vpr, T * K, E, E / R, static_cast<uint4 *>(out));
 }
 
 }  // namespace

@@ -144,18 +144,21 @@ layout_dispatch_kernel(const int32_t *__restrict__ ids, const uint4 *__restrict_
             const int below = (int)((tot[j >> 1] >> (16 * (j & 1))) & 0xffffu);
             sl[j] = (unsigned)tg[j] < (unsigned)E ? below + dup : -1;
         }
-        if (tid < 8 && k0 + tid < k_count) {
+        // the index-map and offset writes go to the block's last warp, which
+        // has the least (at decode sizes often no) copying to do
+        const int wl = tid - (kThreads - 32);
+        if (wl >= 0 && wl < 8 && k0 + wl < k_count) {
             int mine_slot = sl[0];
 #pragma unroll
             for (int j = 1; j < 8; ++j)
-                if (tid == j) mine_slot = sl[j];
-            if (!kRegSlots) slots_s[k0 + tid] = mine_slot;
+                if (wl == j) mine_slot = sl[j];
+            if (!kRegSlots) slots_s[k0 + wl] = mine_slot;
             if (c == 0) {
-                dst_row[mine + k0 + tid] = mine_slot;
+                dst_row[mine + k0 + wl] = mine_slot;
                 if (mine_slot >= 0) src_token[mine_slot] = t;
             }
         }
-        if (role >= 0 && tid == 0) {
+        if (role >= 0 && wl == 8) {
             const int lt = (int)(tot[4] & 0xffffu), eq = (int)(tot[4] >> 16);
             offsets[role] = lt;
             if (role < E) counts[role] = eq;

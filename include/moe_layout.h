@@ -101,8 +101,8 @@ MOE_API size_t moe_layout_workspace_bytes(int32_t T, int32_t K, int32_t E);
  * topk_ids     [T,K] int32, 4-byte aligned.
  * T >= 0, 1 <= K <= min(E, MOE_MAX_TOPK), 1 <= E <= MOE_MAX_EXPERTS,
  * R >= 1 with E % R == 0, T*K < 2^31, and T*K small enough for the kernels'
- * shared memory: at least 1.6 * 10^9 / E entries (1.6 M for E = 1024,
- * 13 M for E = 128); larger batches return MOE_ERR_INVALID_ARG.
+ * shared memory: at least 3.8 * 10^8 / E entries (376 K for E = 1024, 4.2 M
+ * for E = 128); larger batches return MOE_ERR_INVALID_ARG.
  * Outputs (int32, 4-byte aligned): expert_counts, expert_offsets,
  * rank_offsets, src_token, dst_row.  dst_row and src_token may be NULL only
  * when T == 0.
@@ -292,13 +292,13 @@ MOE_API moe_status_t moe_layout_dispatch(const int32_t *topk_ids, const void *to
                                          cudaStream_t stream);
 
 /* Number of kernel launches moe_layout_dispatch makes for these sizes: 1
- * when it runs as a single kernel, otherwise moe_layout's one or three
+ * when it runs as a single kernel, otherwise moe_layout's one or two
  * kernels plus moe_dispatch's one.  0 for invalid sizes. */
 MOE_API int32_t moe_layout_dispatch_kernels(int32_t T, int32_t H, int32_t K,
                                             int32_t E, int32_t fp8);
 
-/* Bytes of the fixed scratch array that moe_layout_static uses (256 KiB). */
-#define MOE_LAYOUT_STATIC_SCRATCH_BYTES (256u << 10)
+/* Bytes of the fixed scratch array that moe_layout_static uses (96 KiB). */
+#define MOE_LAYOUT_STATIC_SCRATCH_BYTES (96u << 10)
 
 /*
  * moe_layout_static -- moe_layout for callers that cannot allocate device
@@ -318,7 +318,7 @@ MOE_API int32_t moe_layout_dispatch_kernels(int32_t T, int32_t H, int32_t K,
  * - Limit: a batch whose moe_layout_workspace_bytes(T,K,E) exceeds
  *   MOE_LAYOUT_STATIC_SCRATCH_BYTES is rejected with MOE_ERR_WORKSPACE.
  *   That covers every batch moe_layout accepts with E >= 2; with E = 1,
- *   batches above about 33 million entries are rejected.
+ *   batches above about 12.5 million entries are rejected.
  * - Set-up: the first call on a device looks up the array's device address
  *   (cudaGetSymbolAddress, with that device current); make that first call
  *   before any stream capture.  Set-up failure returns MOE_ERR_CUDA.

@@ -20,7 +20,7 @@ from combine_moe_layout_05_gb300 import build as moe_build
 from combine_moe_layout_05_gb300 import workload as wl
 
 P, i32 = ctypes.c_void_p, ctypes.c_int32
-SCRATCH_BYTES = 256 << 10
+SCRATCH_BYTES = 96 << 10
 MOE_OK, MOE_ERR_WORKSPACE = 0, 4
 
 
