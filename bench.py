@@ -663,7 +663,7 @@ def run_ours(args):
 def launches_per_step(w, dispatch, unfused, path="packed") -> int:
     """Kernels this library launches per step (mirrors the C ABI's plans)."""
     import combine_moe_layout_05_gb300 as moe
-    layout_kernels = 1 if moe.moe_layout_workspace_bytes(w.T, w.K, w.E) == 0 else 2
+    layout_kernels = 1 if moe.moe_layout_workspace_bytes(w.T, w.K, w.E) == 0 else 3
     if path == "regions":
         return layout_kernels + 3
     if unfused:

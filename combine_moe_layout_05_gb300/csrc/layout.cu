@@ -22,11 +22,11 @@
 //
 // Small batches (T*K <= kSelfMaxEntries) take one launch: each block stages
 // all T*K ids and counts the totals and the entries before its chunk itself.
-// Larger batches take two launches and a workspace, with no block ever
-// waiting for another: a counting kernel writes each chunk's histogram, and
-// every block of the ranking kernel stages all the histograms, sums their
-// columns into the expert totals and the entries before its chunk, scans the
-// totals into the offsets and assigns its chunk's slots.
+// Larger batches take three launches and a workspace, with no block ever
+// waiting for another: a counting kernel writes each chunk's histogram, a
+// one-block kernel turns the histograms into each chunk's first slot per
+// expert and writes the expert offsets, and the ranking kernel assigns the
+// slots.
 #include "common.cuh"
 #include "internal.h"
 #include "layout_common.cuh"
@@ -42,7 +42,8 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kSelfMaxEntries = 4096;
 constexpr int kSelfChunk = 512;
 constexpr int kChunk = 1024;
-constexpr int kScanCells = 16 * 1024;    // chunks x E staged by every ranking block (64 KB)
+constexpr int kScanCells = 16 * 1024;    // chunks x E staged by the scan (64 KB)
+constexpr int kScanThreads = 1024;
 
 // Multi-launch path, kernel 1: histogram and error bits of chunk c.
 // ws_cnt is chunk-major: ws_cnt[c * E + e].
@@ -80,17 +81,86 @@ layout_count_kernel(const int32_t *__restrict__ ids, int T, int K, int E, int tp
     if (tid == 0) ws_err[c] = s_err;
 }
 
-// Ranking.  kSelf: one launch; every block stages all T*K ids and counts the
-// totals and the entries before its chunk itself.  Otherwise every block
-// stages the counting kernel's chunk histograms (chunks x E ints, one memory
-// latency) and sums their columns for the same two quantities.  Either way
-// the block then scans the totals into the expert offsets, and block 0
-// writes the counts, offsets, rank offsets and error word.
+// Multi-launch path, kernel 2 (one block): turns the chunk histograms into
+// each chunk's first slot per expert, in place:
+//     ws_cnt[c * E + e] <- offsets[e] + sum of ws_cnt[c' * E + e], c' < c
+// and writes the counts, offsets, rank offsets and the OR of the error bits.
+// The histograms are staged in shared memory (one memory latency); P
+// threads share each expert's chunks, and the threads of a warp hold
+// consecutive experts, so shared-memory accesses never conflict.
+__global__ void __launch_bounds__(kScanThreads)
+layout_scan_kernel(int E, int R, int chunks, int32_t *__restrict__ ws_cnt,
+                   const uint32_t *__restrict__ ws_err, int32_t *__restrict__ counts,
+                   int32_t *__restrict__ offsets, int32_t *__restrict__ rank_offsets,
+                   uint32_t *__restrict__ dev_error)
+{
+    extern __shared__ __align__(16) int32_t cnt[];   // [chunks][E]
+    __shared__ int32_t part[kScanThreads];           // [P][E] partial sums, then prefixes
+    __shared__ int32_t tot[MOE_MAX_EXPERTS];
+    __shared__ int32_t off[MOE_MAX_EXPERTS + 1];
+    __shared__ int32_t warp_sums[32];
+    __shared__ uint32_t s_err;
+    const int tid = threadIdx.x;
+    const int P = E < kScanThreads ? kScanThreads / E : 1;
+    const int e = tid % E, p = tid / E;
+    const bool mine = p < P;
+    const int per = ceil_div(chunks, P);
+    const int c0 = min(chunks, p * per), c1 = min(chunks, c0 + per);
+    if (tid == 0) s_err = 0;
+    __syncthreads();
+    pdl_wait();
+    pdl_trigger();
+    stage_i32(cnt, ws_cnt, E * chunks);
+    uint32_t err = 0;
+    for (int c = tid; c < chunks; c += kScanThreads) err |= ws_err[c];
+    if (err) atomicOr(&s_err, err);
+    cp_async_wait_all();
+    __syncthreads();
+
+    int sum = 0;
+    if (mine)
+        for (int c = c0; c < c1; ++c) sum += cnt[c * E + e];
+    if (mine) part[p * E + e] = sum;
+    __syncthreads();
+    if (tid < E) {
+        int run = 0;
+        for (int q = 0; q < P; ++q) {
+            const int v = part[q * E + tid];
+            part[q * E + tid] = run;
+            run += v;
+        }
+        tot[tid] = run;
+    }
+    __syncthreads();
+    scan_experts<kScanThreads>(tot, off, E, warp_sums);
+    if (mine) {
+        int run = off[e] + part[p * E + e];
+        for (int c = c0; c < c1; ++c) {
+            const int v = cnt[c * E + e];
+            ws_cnt[(size_t)c * E + e] = run;
+            run += v;
+        }
+    }
+    for (int x = tid; x < E; x += kScanThreads) {
+        counts[x] = tot[x];
+        offsets[x] = off[x];
+    }
+    if (tid == 0) {
+        offsets[E] = off[E];
+        if (dev_error) *dev_error = s_err;
+    }
+    const int epr = E / R;
+    for (int r = tid; r <= R; r += kScanThreads) rank_offsets[r] = off[r * epr];
+}
+
+// Ranking.  kSelf: one launch; every block stages all T*K ids, counts the
+// totals and the entries before its chunk itself, and block 0 writes the
+// counts, offsets, rank offsets and error word.  Otherwise the block's
+// per-expert base comes from the scan kernel's offsets and prefixes.
 template <bool kSelf>
 __global__ void __launch_bounds__(kThreads)
 layout_rank_kernel(const int32_t *__restrict__ ids, int T, int K, int E, int R,
                    int tpc, int chunks, const int32_t *__restrict__ ws_cnt,
-                   const uint32_t *__restrict__ ws_err,
                    int32_t *__restrict__ counts, int32_t *__restrict__ offsets,
                    int32_t *__restrict__ rank_offsets,
                    int32_t *__restrict__ src_token,
@@ -99,10 +169,10 @@ layout_rank_kernel(const int32_t *__restrict__ ids, int T, int K, int E, int R,
     extern __shared__ __align__(16) int32_t sm[];
     int32_t *rows = sm;                          // [kWarps][E] running slots
     int32_t *base = rows + kWarps * E;           // [E + 1]
-    int32_t *total = base + E + 1;               // [E] entries per expert
-    int32_t *before = total + E;                 // [E] entries before this chunk
-    int32_t *cnt = sm + align4(kWarps * E + 3 * E + 1);            // [chunks][E] (!kSelf)
-    int32_t *ids_s = cnt + (kSelf ? 0 : align4(chunks * E));       // 16-byte aligned
+    int32_t *total = base + E + 1;               // [E]      (kSelf)
+    int32_t *before = total + E;                 // [E]      (kSelf)
+    // all entries (kSelf) or the chunk's, 16-byte aligned for the staging copy
+    int32_t *ids_s = sm + align4(kWarps * E + E + 1 + (kSelf ? 2 * E : 0));
     __shared__ int32_t warp_sums[32];
     __shared__ uint32_t s_err;
 
@@ -121,13 +191,8 @@ layout_rank_kernel(const int32_t *__restrict__ ids, int T, int K, int E, int R,
     if (kSelf) {
         stage_i32(ids_s, ids, n);
     } else {
-        stage_i32(cnt, ws_cnt, chunks * E);
         stage_i32(ids_s, ids + first, m);
-        if (c == 0) {
-            uint32_t err = 0;
-            for (int cc = tid; cc < chunks; cc += kThreads) err |= __ldg(ws_err + cc);
-            if (err) atomicOr(&s_err, err);
-        }
+        for (int e = tid; e < E; e += kThreads) base[e] = __ldg(ws_cnt + (size_t)c * E + e);
     }
     cp_async_wait_all();
     __syncthreads();
@@ -145,38 +210,29 @@ layout_rank_kernel(const int32_t *__restrict__ ids, int T, int K, int E, int R,
             const uint32_t err = token_errors(ids_s, T, K, E);
             if (err) atomicOr(&s_err, err);
         }
-    } else {
-        for (int e = tid; e < E; e += kThreads) {
-            int tot = 0, pre = 0;
-            for (int cc = 0; cc < chunks; ++cc) {
-                const int v = cnt[cc * E + e];
-                tot += v;
-                pre += cc < c ? v : 0;
-            }
-            total[e] = tot;
-            before[e] = pre;
-        }
     }
     int lo, hi;
     warp_segment<kWarps>(m, w, lo, hi);
     warp_count(mine, lo, hi, E, lane, rows + w * E);
     __syncthreads();
 
-    scan_experts<kThreads>(total, base, E, warp_sums);
-    if (c == 0) {
-        for (int e = tid; e < E; e += kThreads) {
-            counts[e] = total[e];
-            offsets[e] = base[e];
+    if (kSelf) {
+        scan_experts<kThreads>(total, base, E, warp_sums);
+        if (c == 0) {
+            for (int e = tid; e < E; e += kThreads) {
+                counts[e] = total[e];
+                offsets[e] = base[e];
+            }
+            if (tid == 0) {
+                offsets[E] = base[E];
+                if (dev_error) *dev_error = s_err;
+            }
+            const int epr = E / R;
+            for (int r = tid; r <= R; r += kThreads) rank_offsets[r] = base[r * epr];
         }
-        if (tid == 0) {
-            offsets[E] = base[E];
-            if (dev_error) *dev_error = s_err;
-        }
-        const int epr = E / R;
-        for (int r = tid; r <= R; r += kThreads) rank_offsets[r] = base[r * epr];
     }
     for (int e = tid; e < E; e += kThreads) {
-        int run = base[e] + before[e];
+        int run = base[e] + (kSelf ? before[e] : 0);
 #pragma unroll
         for (int ww = 0; ww < kWarps; ++ww) {
             const int v = rows[ww * E + e];
@@ -190,10 +246,9 @@ layout_rank_kernel(const int32_t *__restrict__ ids, int T, int K, int E, int R,
 
 size_t rank_smem_bytes(const LayoutPlan &p, int T, int K, int E)
 {
-    const size_t head = (size_t)align4(kWarps * E + 3 * E + 1);
-    if (p.single_launch) return sizeof(int32_t) * (head + (size_t)T * K);
-    return sizeof(int32_t) * (head + (size_t)align4(p.chunks * E) +
-                              (size_t)p.tokens_per_chunk * K);
+    const size_t ids = p.single_launch ? (size_t)T * K : (size_t)p.tokens_per_chunk * K;
+    const int extra = p.single_launch ? 2 * E : 0;
+    return sizeof(int32_t) * ((size_t)align4(kWarps * E + E + 1 + extra) + ids);
 }
 
 // Raises a kernel's dynamic shared memory limit to the most the device
@@ -262,7 +317,8 @@ bool layout_supported(int T, int K, int E)
     if (rank_smem_bytes(p, T, K, E) > kLimit) return false;
     if (p.single_launch) return true;
     const size_t count = sizeof(int32_t) * ((size_t)align4(E) + (size_t)p.tokens_per_chunk * K);
-    return count <= kLimit;
+    const size_t scan = sizeof(int32_t) * (size_t)E * p.chunks;
+    return count <= kLimit && scan <= kLimit;
 }
 
 size_t layout_workspace_bytes(const LayoutPlan &plan, int E)
@@ -285,8 +341,8 @@ cudaError_t launch_layout(const int32_t *topk_ids, int T, int K, int E, int R,
         if (e != cudaSuccess) return e;
         return launch_pdl(layout_rank_kernel<true>, dim3(p.chunks), dim3(kThreads), rsmem,
                           stream, topk_ids, T, K, E, R, p.tokens_per_chunk, p.chunks,
-                          (const int32_t *)nullptr, (const uint32_t *)nullptr, expert_counts,
-                          expert_offsets, rank_offsets, src_token, dst_row, dev_error);
+                          (const int32_t *)nullptr, expert_counts, expert_offsets,
+                          rank_offsets, src_token, dst_row, dev_error);
     }
     int32_t *ws_cnt = static_cast<int32_t *>(workspace);
     uint32_t *ws_err = reinterpret_cast<uint32_t *>(ws_cnt + (size_t)p.chunks * E);
@@ -296,12 +352,19 @@ cudaError_t launch_layout(const int32_t *topk_ids, int T, int K, int E, int R,
     e = launch_pdl(layout_count_kernel, dim3(p.chunks), dim3(kThreads), csmem, stream,
                    topk_ids, T, K, E, p.tokens_per_chunk, p.chunks, ws_cnt, ws_err);
     if (e != cudaSuccess) return e;
+    const size_t ssmem = sizeof(int32_t) * (size_t)E * p.chunks;
+    e = allow_smem((const void *)layout_scan_kernel, ssmem);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(layout_scan_kernel, dim3(1), dim3(kScanThreads), ssmem, stream, E, R,
+                   p.chunks, ws_cnt, (const uint32_t *)ws_err, expert_counts,
+                   expert_offsets, rank_offsets, dev_error);
+    if (e != cudaSuccess) return e;
     e = allow_smem((const void *)layout_rank_kernel<false>, rsmem);
     if (e != cudaSuccess) return e;
     return launch_pdl(layout_rank_kernel<false>, dim3(p.chunks), dim3(kThreads), rsmem,
                       stream, topk_ids, T, K, E, R, p.tokens_per_chunk, p.chunks,
-                      (const int32_t *)ws_cnt, (const uint32_t *)ws_err, expert_counts,
-                      expert_offsets, rank_offsets, src_token, dst_row, dev_error);
+                      (const int32_t *)ws_cnt, expert_counts, expert_offsets,
+                      rank_offsets, src_token, dst_row, dev_error);
 }
 
 }  // namespace moe

@@ -101,7 +101,7 @@ MOE_API size_t moe_layout_workspace_bytes(int32_t T, int32_t K, int32_t E);
  * topk_ids     [T,K] int32, 4-byte aligned.
  * T >= 0, 1 <= K <= min(E, MOE_MAX_TOPK), 1 <= E <= MOE_MAX_EXPERTS,
  * R >= 1 with E % R == 0, T*K < 2^31, and T*K small enough for the kernels'
- * shared memory: at least 3.8 * 10^8 / E entries (376 K for E = 1024, 4.2 M
+ * shared memory: at least 6.5 * 10^8 / E entries (671 K for E = 1024, 6.4 M
  * for E = 128); larger batches return MOE_ERR_INVALID_ARG.
  * Outputs (int32, 4-byte aligned): expert_counts, expert_offsets,
  * rank_offsets, src_token, dst_row.  dst_row and src_token may be NULL only
@@ -292,7 +292,7 @@ MOE_API moe_status_t moe_layout_dispatch(const int32_t *topk_ids, const void *to
                                          cudaStream_t stream);
 
 /* Number of kernel launches moe_layout_dispatch makes for these sizes: 1
- * when it runs as a single kernel, otherwise moe_layout's one or two
+ * when it runs as a single kernel, otherwise moe_layout's one or three
  * kernels plus moe_dispatch's one.  0 for invalid sizes. */
 MOE_API int32_t moe_layout_dispatch_kernels(int32_t T, int32_t H, int32_t K,
                                             int32_t E, int32_t fp8);
