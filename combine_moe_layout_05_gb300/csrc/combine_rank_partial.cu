@@ -16,84 +16,92 @@
 namespace moe {
 namespace {
 
-// One thread per block orders the token's valid entries by (rank, k) in
-// shared memory -- slot, weight, and a bit marking the last entry of each
-// rank's group -- so every thread then gathers its 8 values per entry in that
-// order and makes a single pass: fused multiply-adds into the group's
-// partial, and at each group's end the partial rounded to bf16 is added into
-// the fp32 total.  KT > 0: all gathers are issued before any arithmetic.
+// Every warp orders the token's valid entries by (rank, k) itself, with no
+// shared memory and no barrier: lane k (< K) loads entry k's slot, expert and
+// weight, its position in that order is the number of lanes with a smaller
+// key (rank << 5 | k), and a lane whose rank no higher lane shares ends its
+// rank's group.  The order is the same for every warp of the block (one
+// token), so every loop below is warp-uniform.  Each thread then gathers its
+// 8 values of every entry in that order -- the source lane of position p is
+// found with a ballot and the slot and weight are shuffled from it -- and
+// makes a single pass: fused multiply-adds into the group's partial, and at
+// each group's end the partial rounded to bf16 is added into the fp32 total.
+// Up to KT (or kBatch) gathers are in flight before any arithmetic.
 template <int KT>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 4)   // 4 blocks per SM: the decode grid in one wave
 combine_rank_partial_kernel(const uint4 *__restrict__ y, const float *__restrict__ weights,
                             const int32_t *__restrict__ ids, const int32_t *__restrict__ dst_row,
                             int K, int vpr, int rows, int E, int epr, uint4 *__restrict__ out)
 {
-    __shared__ int32_t s_row[MOE_MAX_TOPK];
-    __shared__ float s_w[MOE_MAX_TOPK];
-    __shared__ uint32_t s_last;
-    __shared__ int32_t s_n;
     pdl_wait();
     pdl_trigger();
     const int t = blockIdx.x;
     const int v = blockIdx.y * blockDim.x + threadIdx.x;
+    const bool active = v < vpr;            // inactive lanes still take part in the collectives
+    const int lane = threadIdx.x & 31;
     const int k_count = KT > 0 ? KT : K;
-    if (threadIdx.x == 0) {
-        int key[MOE_MAX_TOPK];
-        int n = 0;
-        for (int k = 0; k < k_count; ++k) {
-            const int r = __ldg(dst_row + (size_t)t * k_count + k);
-            const int e = __ldg(ids + (size_t)t * k_count + k);
-            if ((unsigned)r < (unsigned)rows && (unsigned)e < (unsigned)E)
-                key[n++] = ((e / epr) << 5) | k;          // rank major, then k
+
+    int row = 0, key = 0x7fffffff, group = 0x40000000 | lane;
+    float wt = 0.0f;
+    bool valid = false;
+    if (lane < k_count) {
+        row = __ldg(dst_row + (size_t)t * k_count + lane);
+        const int e = __ldg(ids + (size_t)t * k_count + lane);
+        wt = __ldg(weights + (size_t)t * k_count + lane);
+        valid = (unsigned)row < (unsigned)rows && (unsigned)e < (unsigned)E;
+        if (valid) {
+            group = e / epr;
+            key = (group << 5) | lane;      // rank major, then k
         }
-        for (int i = 1; i < n; ++i) {                     // insertion sort, n <= 32
-            const int x = key[i];
-            int j = i - 1;
-            while (j >= 0 && key[j] > x) {
-                key[j + 1] = key[j];
-                --j;
-            }
-            key[j + 1] = x;
-        }
-        uint32_t last = 0;
-        for (int i = 0; i < n; ++i) {
-            const int k = key[i] & 31;
-            s_row[i] = __ldg(dst_row + (size_t)t * k_count + k);
-            s_w[i] = __ldg(weights + (size_t)t * k_count + k);
-            if (i == n - 1 || (key[i] >> 5) != (key[i + 1] >> 5)) last |= 1u << i;
-        }
-        s_last = last;
-        s_n = n;
     }
-    __syncthreads();
-    if (v >= vpr) return;
-    const int n = s_n;
-    const uint32_t last = s_last;
+    int pos = 0;
+    if (KT > 0) {
+#pragma unroll
+        for (int j = 0; j < (KT > 0 ? KT : 1); ++j) pos += __shfl_sync(kFullMask, key, j) < key;
+    } else {
+        for (int j = 0; j < k_count; ++j) pos += __shfl_sync(kFullMask, key, j) < key;
+    }
+    const uint32_t valid_mask = __ballot_sync(kFullMask, valid);
+    const int n = __popc(valid_mask);
+    const uint32_t same = __match_any_sync(kFullMask, group);
+    const bool ends = valid && (same & ~((2u << lane) - 1u)) == 0u;
+    const uint32_t last = __reduce_or_sync(kFullMask, ends ? 1u << pos : 0u);
 
     float total[8], part[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) total[j] = part[j] = 0.0f;
-    auto step = [&](int i, const uint4 &val) {
-        fma8(part, s_w[i], val);
-        if ((last >> i) & 1u) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                total[j] = __fadd_rn(total[j], __bfloat162float(__float2bfloat16_rn(part[j])));
-                part[j] = 0.0f;
-            }
-        }
-    };
     constexpr int B = KT > 0 ? KT : kBatch;
-    for (int i0 = 0; i0 < n; i0 += B) {
+    // source lane of position p (0 when p >= n)
+    auto lane_of = [&](int p) {
+        const uint32_t at = __ballot_sync(kFullMask, valid && pos == p);
+        return at ? __ffs(at) - 1 : 0;
+    };
+    for (int p0 = 0; p0 < n; p0 += B) {
         uint4 val[B];
 #pragma unroll
-        for (int i = 0; i < B; ++i)
-            val[i] = i0 + i < n ? ld_stream_v4(y + (size_t)s_row[i0 + i] * vpr + v)
-                                : make_uint4(0, 0, 0, 0);
+        for (int i = 0; i < B; ++i) {
+            const int p = p0 + i;
+            const int r = __shfl_sync(kFullMask, row, lane_of(p));
+            val[i] = (p < n && active) ? ld_stream_v4(y + (size_t)r * vpr + v)
+                                       : make_uint4(0, 0, 0, 0);
+        }
 #pragma unroll
-        for (int i = 0; i < B; ++i)
-            if (i0 + i < n) step(i0 + i, val[i]);
+        for (int i = 0; i < B; ++i) {
+            const int p = p0 + i;
+            if (p < n) {                    // warp-uniform
+                fma8(part, __shfl_sync(kFullMask, wt, lane_of(p)), val[i]);
+                if ((last >> p) & 1u) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        total[j] = __fadd_rn(total[j],
+                                             __bfloat162float(__float2bfloat16_rn(part[j])));
+                        part[j] = 0.0f;
+                    }
+                }
+            }
+        }
     }
+    if (!active) return;
     uint4 o;
     o.x = pack_bf16x2_rn(total[0], total[1]);
     o.y = pack_bf16x2_rn(total[2], total[3]);

@@ -14,8 +14,9 @@
 //
 // send: like the dispatch kernels (block = one token x a slice of its row,
 // each token piece read once), but each of the K stores goes to the region
-// row of its slot.  recv: block = one packed row x a slice; the row's rank
-// is found by binary search of rank_offsets.
+// row of its slot.  recv: block = one packed row x a slice, 4 vectors of 16
+// bytes per thread; the row's rank is found by binary search of
+// rank_offsets.
 #include "common.cuh"
 #include "internal.h"
 #include "moe_layout.h"
@@ -23,6 +24,8 @@
 
 namespace moe {
 namespace {
+
+constexpr int kRecvVecs = 4;
 
 // Region row of slot s whose expert e is valid, as (base, row); false when
 // the slot falls past the bulk capacity.
@@ -136,9 +139,19 @@ dispatch_recv_kernel(const uint8_t *__restrict__ priv, const float *__restrict__
     }
     const size_t row_bytes = kFp8 ? (size_t)H : (size_t)H * 2;
     const int vecs = (int)(row_bytes >> 4);
-    for (int v = blockIdx.y * blockDim.x + threadIdx.x; v < vecs; v += gridDim.y * blockDim.x)
-        st_v4(packed + (size_t)row * row_bytes + (size_t)v * 16,
-              ld_stream_v4(src + srow * row_bytes + (size_t)v * 16));
+    // kRecvVecs 16-byte vectors per thread, all loads issued before the stores
+    const int v0 = blockIdx.y * blockDim.x * kRecvVecs + threadIdx.x;
+    uint4 val[kRecvVecs];
+#pragma unroll
+    for (int j = 0; j < kRecvVecs; ++j) {
+        const int v = v0 + j * blockDim.x;
+        if (v < vecs) val[j] = ld_stream_v4(src + srow * row_bytes + (size_t)v * 16);
+    }
+#pragma unroll
+    for (int j = 0; j < kRecvVecs; ++j) {
+        const int v = v0 + j * blockDim.x;
+        if (v < vecs) st_v4(packed + (size_t)row * row_bytes + (size_t)v * 16, val[j]);
+    }
     if (kFp8) {
         const int nb = H >> 7;
         for (int j = blockIdx.y * blockDim.x + threadIdx.x; j < nb; j += gridDim.y * blockDim.x)
@@ -174,8 +187,8 @@ cudaError_t launch_dispatch_recv(const void *priv, const float *priv_scales, int
                                  int fp8, void *packed, float *scales, cudaStream_t stream)
 {
     const int vecs = fp8 ? H / 16 : H / 8;
-    const int threads = pick_row_block(vecs);
-    const dim3 grid(T * K, ceil_div(vecs, threads));
+    const int threads = pick_row_block(ceil_div(vecs, kRecvVecs));
+    const dim3 grid(T * K, ceil_div(vecs, threads * kRecvVecs));
     if (fp8)
         return launch_pdl(dispatch_recv_kernel<true>, grid, dim3(threads), 0, stream,
                           static_cast<const uint8_t *>(priv), priv_scales,

@@ -72,3 +72,26 @@ def test_rank_partial_order_sensitive(oracle):
         w = np.ones((1, 3), np.float32)
         got = gpu_rank_partial(yb, w, ids[:1] if R == 3 else ids[1:], lay.dst_row, 6, R)
         assert np.all(wl.bf16_bits_to_f32(got) == 1.0)
+
+
+@pytest.mark.parametrize("K", [3, 8, 32])
+def test_rank_partial_invalid_entries(oracle, K):
+    """Entries with a bad expert id or an out-of-range slot are skipped, wherever
+    they fall in the (rank, k) order; a token with no valid entry gives +0."""
+    T, H, E, R = 40, 264, 64, 8
+    rng = np.random.default_rng(K)
+    ids = wl.routing_uniform(T, E, K, rng)
+    ids[rng.random((T, K)) < 0.2] = -1
+    ids[3, :] = E + 5                                   # no valid entry at all
+    ids[5, 0] = E
+    lay = oracle.layout(ids, E, R)
+    dst = lay.dst_row.copy()
+    ok = np.argwhere(dst >= 0)
+    for t, k in ok[rng.choice(len(ok), 6, replace=False)]:
+        dst[t, k] = T * K + int(rng.integers(0, 3))     # valid id, slot past the rows
+    y = wl.to_bf16_bits(rng.standard_normal((T * K, H)).astype(np.float32))
+    wts = rng.standard_normal((T, K)).astype(np.float32)
+    got = gpu_rank_partial(y, wts, ids, dst, E, R)
+    exp = oracle.combine_rank_partial(y, wts, ids, dst, E, R)
+    assert np.array_equal(got, exp)
+    assert np.all(got[3] == 0)
