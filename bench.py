@@ -116,6 +116,22 @@ def read_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def host_info() -> dict:
+    """The host the CPU baseline ran on: logical CPUs and the CPU model."""
+    model = None
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key, _, val = line.partition(":")
+                if key.strip() in ("model name", "Model", "Hardware"):
+                    model = val.strip()
+                    break
+    except OSError:
+        pass
+    import platform
+    return {"host_cpus": os.cpu_count(), "cpu_model": model or platform.machine()}
+
+
 def algorithmic_bytes(w, dispatch: str):
     """Bytes each kernel must move at minimum for one batch (one launch)."""
     T, H, K, E, R = w.T, w.H, w.K, w.E, w.R
@@ -621,6 +637,7 @@ def run_ours(args):
     if rank == 0 and not args.no_cpu_baseline and world == 1:
         tps, tsamp, nst = time_oracle(w, dispatch, inp, y_bits, args.cpu_seconds, combine=args.combine)
         cpu = {"value": round(tps, 1), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+               **host_info(),
                "sample": f"{nst} oracle steps of the full {w.name} batch "
                          f"(T={tsamp}), single thread, {args.cpu_seconds:.0f} s budget"}
 
@@ -792,7 +809,7 @@ def run_reference(args):
         "config": {"workload": w.name, "T": w.T, "H": w.H, "E": w.E, "R": w.R, "K": w.K,
                    "dispatch": dispatch, "sample_tokens_per_step": T_s},
         "cpu_baseline": {"value": round(value, 1), "unit": "tokens/s", "cores": 1,
-                         "kind": "oracle", "sample": sample},
+                         "kind": "oracle", "sample": sample, **host_info()},
         "e2e": {"value": round(value, 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)

@@ -87,5 +87,6 @@ def test_reference_arm_runs_on_cpu():
     line = json.loads(r.stdout.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
+    assert line["cpu_baseline"]["host_cpus"] >= 1 and line["cpu_baseline"]["cpu_model"]
     assert line["e2e"]["h2d_bytes_per_step"] == 0
     assert line["metric"] == bench.METRIC
