@@ -20,13 +20,14 @@ namespace {
 // shared memory and no barrier: lane k (< K) loads entry k's slot, expert and
 // weight, its position in that order is the number of lanes with a smaller
 // key (rank << 5 | k), and a lane whose rank no higher lane shares ends its
-// rank's group.  The order is the same for every warp of the block (one
-// token), so every loop below is warp-uniform.  Each thread then gathers its
-// 8 values of every entry in that order -- the source lane of position p is
-// found with a ballot and the slot and weight are shuffled from it -- and
-// makes a single pass: fused multiply-adds into the group's partial, and at
-// each group's end the partial rounded to bf16 is added into the fp32 total.
-// Up to KT (or kBatch) gathers are in flight before any arithmetic.
+// rank's group.  Lane p then fetches the slot and weight of the entry at
+// position p, so each position costs two shuffles later.  The order is the
+// same for every warp of the block (one token), so every loop below is
+// warp-uniform.  Each thread gathers its 8 values of every entry in that
+// order and makes a single pass: fused multiply-adds into the group's
+// partial, and at each group's end the partial rounded to bf16 (two values
+// per conversion) is added into the fp32 total.  Up to KT (or kBatch)
+// gathers are in flight before any arithmetic.
 template <int KT>
 __global__ void __launch_bounds__(256, 4)   // 4 blocks per SM: the decode grid in one wave
 combine_rank_partial_kernel(const uint4 *__restrict__ y, const float *__restrict__ weights,
@@ -55,33 +56,32 @@ combine_rank_partial_kernel(const uint4 *__restrict__ y, const float *__restrict
         }
     }
     int pos = 0;
-    if (KT > 0) {
 #pragma unroll
-        for (int j = 0; j < (KT > 0 ? KT : 1); ++j) pos += __shfl_sync(kFullMask, key, j) < key;
-    } else {
-        for (int j = 0; j < k_count; ++j) pos += __shfl_sync(kFullMask, key, j) < key;
-    }
-    const uint32_t valid_mask = __ballot_sync(kFullMask, valid);
-    const int n = __popc(valid_mask);
+    for (int j = 0; j < (KT > 0 ? KT : MOE_MAX_TOPK); ++j)
+        if (KT > 0 || j < k_count) pos += __shfl_sync(kFullMask, key, j) < key;
+    const int n = __popc(__ballot_sync(kFullMask, valid));
     const uint32_t same = __match_any_sync(kFullMask, group);
     const bool ends = valid && (same & ~((2u << lane) - 1u)) == 0u;
     const uint32_t last = __reduce_or_sync(kFullMask, ends ? 1u << pos : 0u);
+    // lane p <- the entry at position p (lanes p >= n keep lane 0's, unused)
+    const int at = valid ? pos : -1;
+    int src = 0;
+#pragma unroll
+    for (int j = 0; j < (KT > 0 ? KT : MOE_MAX_TOPK); ++j)
+        if (KT > 0 || j < k_count) src = __shfl_sync(kFullMask, at, j) == lane ? j : src;
+    const int row_p = __shfl_sync(kFullMask, row, src);
+    const float wt_p = __shfl_sync(kFullMask, wt, src);
 
     float total[8], part[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) total[j] = part[j] = 0.0f;
     constexpr int B = KT > 0 ? KT : kBatch;
-    // source lane of position p (0 when p >= n)
-    auto lane_of = [&](int p) {
-        const uint32_t at = __ballot_sync(kFullMask, valid && pos == p);
-        return at ? __ffs(at) - 1 : 0;
-    };
     for (int p0 = 0; p0 < n; p0 += B) {
         uint4 val[B];
 #pragma unroll
         for (int i = 0; i < B; ++i) {
             const int p = p0 + i;
-            const int r = __shfl_sync(kFullMask, row, lane_of(p));
+            const int r = __shfl_sync(kFullMask, row_p, p & 31);
             val[i] = (p < n && active) ? ld_stream_v4(y + (size_t)r * vpr + v)
                                        : make_uint4(0, 0, 0, 0);
         }
@@ -89,13 +89,14 @@ combine_rank_partial_kernel(const uint4 *__restrict__ y, const float *__restrict
         for (int i = 0; i < B; ++i) {
             const int p = p0 + i;
             if (p < n) {                    // warp-uniform
-                fma8(part, __shfl_sync(kFullMask, wt, lane_of(p)), val[i]);
+                fma8(part, __shfl_sync(kFullMask, wt_p, p & 31), val[i]);
                 if ((last >> p) & 1u) {
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        total[j] = __fadd_rn(total[j],
-                                             __bfloat162float(__float2bfloat16_rn(part[j])));
-                        part[j] = 0.0f;
+                    for (int j = 0; j < 8; j += 2) {
+                        const uint32_t h = pack_bf16x2_rn(part[j], part[j + 1]);
+                        total[j] = __fadd_rn(total[j], __uint_as_float(h << 16));
+                        total[j + 1] = __fadd_rn(total[j + 1], __uint_as_float(h & 0xffff0000u));
+                        part[j] = part[j + 1] = 0.0f;
                     }
                 }
             }
