@@ -16,6 +16,16 @@
 namespace moe {
 namespace {
 
+// lo += f32(low bf16 of h), hi += f32(high bf16 of h), each an IEEE fp32 add
+// rounded to nearest even: the mixed-precision add widens the bf16 operand
+// exactly, so this equals __fadd_rn on the widened value, in one instruction.
+__device__ __forceinline__ void add_bf16x2_rn(float &lo, float &hi, uint32_t h)
+{
+    asm("{\n\t.reg .b16 l, u;\n\tmov.b32 {l, u}, %2;\n\t"
+        "add.rn.f32.bf16 %0, l, %0;\n\tadd.rn.f32.bf16 %1, u, %1;\n\t}"
+        : "+f"(lo), "+f"(hi) : "r"(h));
+}
+
 // Every warp orders the token's valid entries by (rank, k) itself, with no
 // shared memory and no barrier: lane k (< K) loads entry k's slot, expert and
 // weight, its position in that order is the number of lanes with a smaller
@@ -26,8 +36,8 @@ namespace {
 // warp-uniform.  Each thread gathers its 8 values of every entry in that
 // order and makes a single pass: fused multiply-adds into the group's
 // partial, and at each group's end the partial rounded to bf16 (two values
-// per conversion) is added into the fp32 total.  Up to KT (or kBatch)
-// gathers are in flight before any arithmetic.
+// per conversion) is added into the fp32 total with a mixed bf16 + fp32
+// add.  Up to KT (or kBatch) gathers are in flight before any arithmetic.
 template <int KT>
 __global__ void __launch_bounds__(256, 4)   // 4 blocks per SM: the decode grid in one wave
 combine_rank_partial_kernel(const uint4 *__restrict__ y, const float *__restrict__ weights,
@@ -93,9 +103,8 @@ combine_rank_partial_kernel(const uint4 *__restrict__ y, const float *__restrict
                 if ((last >> p) & 1u) {
 #pragma unroll
                     for (int j = 0; j < 8; j += 2) {
-                        const uint32_t h = pack_bf16x2_rn(part[j], part[j + 1]);
-                        total[j] = __fadd_rn(total[j], __uint_as_float(h << 16));
-                        total[j + 1] = __fadd_rn(total[j + 1], __uint_as_float(h & 0xffff0000u));
+                        add_bf16x2_rn(total[j], total[j + 1],
+                                      pack_bf16x2_rn(part[j], part[j + 1]));
                         part[j] = part[j + 1] = 0.0f;
                     }
                 }
