@@ -14,9 +14,10 @@
 //    expert e, the valid ids below e (that is offsets[e]), the entries of e
 //    before token t and the earlier k' of token t with id e; their sum is
 //    the slot, the same stable order as moe_layout.  One pass over the ids
-//    with the counters packed two to a word, a warp reduction and one
-//    barrier, after which every thread adds the warps' partial sums itself
-//    and holds the slots in registers; no histogram, no scan, no atomics;
+//    with the counters packed two to a word (two fp16 lanes per compare for
+//    larger batches), a warp reduction and one barrier, after which every
+//    thread adds the warps' partial sums itself and holds the slots in
+//    registers; no histogram, no scan, no atomics;
 //  * the row slice is requested first, so its HBM latency overlaps the
 //    counting;
 //  * slice 0 of each token writes its dst_row / src_token entries; block b
@@ -24,7 +25,9 @@
 //    starts a rank), and block 0 writes the error word.
 // Each block reads all T*K ids, so this path is used only while blocks x
 // entries stays small (decode shapes); the C ABI falls back to moe_layout +
-// moe_dispatch otherwise.
+// moe_dispatch otherwise.  (A form for larger batches, in which each packing
+// block counted only its layout chunk's earlier ids after the counting and
+// scan kernels, replacing the ranking kernel, measured 25-50 % slower.)
 #include "common.cuh"
 #include "internal.h"
 #include "layout_common.cuh"
@@ -52,7 +55,44 @@ __device__ __forceinline__ void count_entry(int x, int i, int mine, int E, int r
     v[4] += (uint32_t)(x < role) | ((uint32_t)(x == role) << 16);
 }
 
-template <int KT, bool kFp8>
+// Batches of at least kHalfCountMin entries count on packed fp16 pairs
+// instead: an id x (0 <= x < E <= 1024) is the fp16 value 1024 + x, exact
+// and ordered like the ids, and an invalid id is 2048, above every valid one,
+// so one half2 compare tests two targets.  The fp16 sums stay exact: a
+// thread sees at most kMaxEntries / kThreads = 32 entries.  (With fewer
+// entries per thread the integer form is as fast.)
+constexpr int kHalfCountMin = 2048;
+
+__device__ __forceinline__ uint32_t enc_id(int x, int E)
+{
+    return 0x6400u + ((unsigned)x < (unsigned)E ? (uint32_t)x : 1024u);
+}
+
+__device__ __forceinline__ __half2 bits_h2(uint32_t u)
+{
+    return *reinterpret_cast<const __half2 *>(&u);
+}
+
+// count_entry on fp16 pairs: target pair q gains, per half,
+// (x < tg) | (x == tg & before); the role pair gains (x < role, x == role).
+__device__ __forceinline__ void count_entry_h2(int x, bool before, int E,
+                                               const __half2 (&tg2)[4], __half2 role2,
+                                               __half2 (&acc)[5])
+{
+    const __half2 xh = bits_h2(enc_id(x, E) * 0x10001u);
+    const __half2 bm = before ? __float2half2_rn(1.0f) : __float2half2_rn(0.0f);
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        acc[q] = __hadd2(acc[q], __hfma2(__heq2(xh, tg2[q]), bm, __hlt2(xh, tg2[q])));
+    const __half2 lt = __hlt2(xh, role2), eq = __heq2(xh, role2);
+    acc[4] = __hadd2(acc[4], __halves2half2(__low2half(lt), __high2half(eq)));
+}
+
+// Counting modes, fixed at compile time so each kernel holds one path:
+// integer counters or fp16 pairs.
+enum CountMode { kCountInt, kCountHalf };
+
+template <int KT, bool kFp8, int kMode>
 __global__ void __launch_bounds__(kThreads)
 layout_dispatch_kernel(const int32_t *__restrict__ ids, const uint4 *__restrict__ tokens,
                        int T, int H, int K, int E, int R, int chunks, int upc,
@@ -113,7 +153,33 @@ layout_dispatch_kernel(const int32_t *__restrict__ ids, const uint4 *__restrict_
         for (int j = 0; j < 8; ++j) tg[j] = k0 + j < k_count ? __ldg(ids + mine + k0 + j) : -1;
         const int role = (k0 == 0 && b <= E) ? b : -1;
         uint32_t v[5] = {0, 0, 0, 0, 0};
-        if (vec_ids) {
+        if (kMode == kCountHalf) {
+            __half2 tg2[4], acc[5];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                tg2[q] = bits_h2(enc_id(tg[2 * q], E) | enc_id(tg[2 * q + 1], E) << 16);
+            const __half2 role2 = bits_h2(role >= 0 ? (0x6400u + (uint32_t)role) * 0x10001u : 0u);
+#pragma unroll
+            for (int q = 0; q < 5; ++q) acc[q] = __float2half2_rn(0.0f);
+            if (vec_ids) {
+                for (int i = 4 * tid; i < n; i += 4 * kThreads) {
+                    const int4 q = __ldg(reinterpret_cast<const int4 *>(ids + i));
+                    count_entry_h2(q.x, i < mine, E, tg2, role2, acc);
+                    count_entry_h2(q.y, i + 1 < mine, E, tg2, role2, acc);
+                    count_entry_h2(q.z, i + 2 < mine, E, tg2, role2, acc);
+                    count_entry_h2(q.w, i + 3 < mine, E, tg2, role2, acc);
+                }
+            } else {
+                for (int i = tid; i < n; i += kThreads)
+                    count_entry_h2(__ldg(ids + i), i < mine, E, tg2, role2, acc);
+            }
+            // counts c <= 32 to packed 16-bit integers: 1024 + c has bits 0x6400 + c
+#pragma unroll
+            for (int q = 0; q < 5; ++q) {
+                const __half2 h = __hadd2(acc[q], __float2half2_rn(1024.0f));
+                v[q] = *reinterpret_cast<const uint32_t *>(&h) - 0x64006400u;
+            }
+        } else if (vec_ids) {
             for (int i = 4 * tid; i < n; i += 4 * kThreads) {
                 const int4 q = __ldg(reinterpret_cast<const int4 *>(ids + i));
                 count_entry(q.x, i, mine, E, role, tg, v);
@@ -251,30 +317,30 @@ FusedPlan plan_fused(int T, int H, int K, bool fp8)
     return {use, chunks, upc};
 }
 
-template <int KT, bool kFp8>
+template <int KT, bool kFp8, int kMode>
 cudaError_t run_fused(const FusedPlan &p, const int32_t *ids, const void *tokens,
                       int T, int H, int K, int E, int R, int32_t *counts,
                       int32_t *offsets, int32_t *rank_offsets, int32_t *src_token,
                       int32_t *dst_row, uint32_t *dev_error, void *packed,
                       float *scales, cudaStream_t s)
 {
-    return launch_pdl(layout_dispatch_kernel<KT, kFp8>, dim3(T * p.chunks), dim3(kThreads),
-                      0, s, ids, static_cast<const uint4 *>(tokens), T, H, K, E, R,
-                      p.chunks, p.upc, counts, offsets, rank_offsets, src_token,
+    return launch_pdl(layout_dispatch_kernel<KT, kFp8, kMode>, dim3(T * p.chunks),
+                      dim3(kThreads), 0, s, ids, static_cast<const uint4 *>(tokens), T, H, K,
+                      E, R, p.chunks, p.upc, counts, offsets, rank_offsets, src_token,
                       dst_row, dev_error, static_cast<uint8_t *>(packed), scales);
 }
 
-template <bool kFp8>
+template <bool kFp8, int kMode>
 cudaError_t run_fused_k(const FusedPlan &p, const int32_t *ids, const void *tokens,
                         int T, int H, int K, int E, int R, int32_t *counts,
                         int32_t *offsets, int32_t *rank_offsets, int32_t *src_token,
                         int32_t *dst_row, uint32_t *dev_error, void *packed,
                         float *scales, cudaStream_t s)
 {
-#define MOE_FUSED_CASE(KV)                                                          \
-    return run_fused<KV, kFp8>(p, ids, tokens, T, H, K, E, R, counts, offsets,      \
-                               rank_offsets, src_token, dst_row, dev_error, packed, \
-                               scales, s)
+#define MOE_FUSED_CASE(KV)                                                             \
+    return run_fused<KV, kFp8, kMode>(p, ids, tokens, T, H, K, E, R, counts, offsets,    \
+                                         rank_offsets, src_token, dst_row, dev_error,    \
+                                         packed, scales, s)
     switch (K) {
     case 1: MOE_FUSED_CASE(1);
     case 2: MOE_FUSED_CASE(2);
@@ -303,13 +369,18 @@ cudaError_t launch_layout_dispatch(const int32_t *topk_ids, const void *tokens,
 {
     const FusedPlan p = plan_fused(T, H, K, fp8 != 0);
     if (p.use) {
-        if (fp8)
-            return run_fused_k<true>(p, topk_ids, tokens, T, H, K, E, R, expert_counts,
-                                     expert_offsets, rank_offsets, src_token, dst_row,
-                                     dev_error, packed, scales, stream);
-        return run_fused_k<false>(p, topk_ids, tokens, T, H, K, E, R, expert_counts,
-                                  expert_offsets, rank_offsets, src_token, dst_row,
-                                  dev_error, packed, scales, stream);
+#define MOE_FUSED_RUN(F, M)                                                                 \
+    return run_fused_k<F, M>(p, topk_ids, tokens, T, H, K, E, R, expert_counts, expert_offsets, \
+                             rank_offsets, src_token, dst_row, dev_error, packed, scales,       \
+                             stream)
+        const bool half = (long long)T * K >= kHalfCountMin;
+        if (fp8) {
+            if (half) MOE_FUSED_RUN(true, kCountHalf);
+            MOE_FUSED_RUN(true, kCountInt);
+        }
+        if (half) MOE_FUSED_RUN(false, kCountHalf);
+        MOE_FUSED_RUN(false, kCountInt);
+#undef MOE_FUSED_RUN
     }
     cudaError_t e = launch_layout(topk_ids, T, K, E, R, expert_counts, expert_offsets,
                                   rank_offsets, src_token, dst_row, dev_error,

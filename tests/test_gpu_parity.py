@@ -284,6 +284,10 @@ FUSED_SHAPES = [  # T, H, K, E, R, fp8: single-kernel sizes, then fallbacks
     (256, 7168, 8, 256, 32, 1), (128, 7168, 8, 256, 32, 1), (100, 1032, 6, 64, 8, 0),
     (64, 256, 2, 8, 2, 1), (37, 4096, 32, 1024, 16, 0), (250, 384, 9, 1024, 4, 1),
     (1024, 7168, 8, 256, 32, 0), (4096, 7168, 8, 384, 48, 1), (0, 128, 4, 16, 4, 0),
+    # multi-launch layout (T*K > 4096): odd K, runtime K, E = 1024, and chunks
+    # capped by the scan (15000 ids per chunk)
+    (5000, 264, 3, 40, 8, 0), (700, 1024, 9, 64, 4, 1), (600, 512, 32, 1024, 16, 0),
+    (30000, 128, 8, 1024, 32, 0),
 ]
 
 
@@ -342,13 +346,18 @@ def test_layout_dispatch_full_size(oracle, name):
             assert np.array_equal(bf16_host(packed), oracle.dispatch_bf16(inp.tokens, ref.dst_row))
 
 
-def test_layout_dispatch_bad_ids(oracle):
-    """Errors and -1 slots from the single-kernel path match the oracle's."""
-    rng = np.random.default_rng(1)
-    T, H, K, E, R = 50, 256, 4, 16, 4
+@pytest.mark.parametrize("T,K,E,R", [(50, 4, 16, 4), (300, 8, 64, 8), (261, 8, 1024, 32),
+                                     (1500, 4, 16, 4)])
+def test_layout_dispatch_bad_ids(oracle, T, K, E, R):
+    """Errors and -1 slots match the oracle's: single kernel with integer and
+    with fp16 counters (T*K >= 2048), and the multi-launch form (T*K > 4096)."""
+    rng = np.random.default_rng(T)
+    H = 256
     ids = wl.routing_uniform(T, E, K, rng)
     ids[0, 0] = E + 3
     ids[9, 3] = ids[9, 1]
+    ids[T - 1, K - 1] = -1
+    ids[T // 2, 0] = E
     x = wl.to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32))
     ref = oracle.layout(ids, E, R)
     buf = moe.LayoutBuffers(T, K, E, R)
