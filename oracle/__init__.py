@@ -62,8 +62,6 @@ def _load():
             i32 = ctypes.c_int32
             lib.oracle_bf16_to_f32.argtypes = [ctypes.c_uint16]
             lib.oracle_bf16_to_f32.restype = ctypes.c_float
-            lib.oracle_f32_to_bf16.argtypes = [ctypes.c_float]
-            lib.oracle_f32_to_bf16.restype = ctypes.c_uint16
             lib.oracle_e4m3_to_f32.argtypes = [ctypes.c_uint8]
             lib.oracle_e4m3_to_f32.restype = ctypes.c_float
             lib.oracle_f32_to_e4m3_satfinite.argtypes = [ctypes.c_float]
@@ -105,10 +103,6 @@ def _c(a, dtype) -> np.ndarray:
 
 def bf16_to_f32(h: int) -> float:
     return float(_load().oracle_bf16_to_f32(int(h)))
-
-
-def f32_to_bf16(f: float) -> int:
-    return int(_load().oracle_f32_to_bf16(float(np.float32(f))))
 
 
 def e4m3_to_f32(c: int) -> float:
@@ -240,11 +234,6 @@ def combine_rank_partial(y_bits: np.ndarray, topk_weights: np.ndarray,
     _load().oracle_combine_rank_partial(_ptr(y), _ptr(w), _ptr(ids), _ptr(d), T, H, K,
                                         E, R, _ptr(out))
     return out
-
-
-def _rows_u8(a):
-    a = np.ascontiguousarray(a)
-    return a.reshape(a.shape[0], -1).view(np.uint8)
 
 
 def dispatch_send(packed: np.ndarray, scales, rank_offsets: np.ndarray, P: int, C: int):
