@@ -3,6 +3,8 @@ public header declares, and rejects bad arguments on the host before touching
 a GPU (these checks return before any CUDA call, so they run without one)."""
 import ctypes
 import os
+import subprocess
+import sys
 
 import pytest
 
@@ -154,3 +156,24 @@ def test_combine_rank_partial_host_checks(lib):
     assert c(*args(y=FAKE + 8)) == 2
     assert c(*args(ids=FAKE + 2)) == 2
     assert c(None, None, None, None, 0, 64, 2, 8, 2, None, None) == 0
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    """No CPU fallback: without the CUDA library every entry point raises."""
+    missing = str(tmp_path / "libmoe_layout.so")
+    code = (
+        "import sys\n"
+        "from combine_moe_layout_05_gb300 import build, _binding\n"
+        f"build.LIB_PATH = {missing!r}\n"
+        "import combine_moe_layout_05_gb300 as moe\n"
+        "for call in (lambda: moe.load(), lambda: moe.moe_layout_workspace_bytes(8, 2, 4)):\n"
+        "    try:\n"
+        "        call()\n"
+        "    except RuntimeError as e:\n"
+        "        assert 'missing' in str(e), e\n"
+        "    else:\n"
+        "        sys.exit('no error')\n"
+    )
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True,
+                       timeout=120)
+    assert r.returncode == 0, r.stderr + r.stdout
