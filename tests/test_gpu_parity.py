@@ -226,6 +226,50 @@ def test_combine_fma_and_order_sensitive(oracle):
     assert np.all(exp[2] == 0)                       # +0, not -0
 
 
+@pytest.mark.parametrize("K", [3, 8, 9])
+def test_combine_skips_invalid_slots(oracle, K):
+    """Entries whose slot is -1 or past the last row add nothing, on the
+    compile-time-K path (8) and the runtime-K paths (3, and 9 in batches)."""
+    T, H = 40, 264
+    rng = np.random.default_rng(K + 100)
+    y = wl.to_bf16_bits(rng.standard_normal((T * K, H)).astype(np.float32))
+    wts = rng.standard_normal((T, K)).astype(np.float32)
+    dst = rng.permutation(T * K).astype(np.int32).reshape(T, K)
+    dst[rng.random((T, K)) < 0.2] = -1
+    dst[5, :] = -1                                      # a token with no valid entry
+    dst[6, K - 1] = T * K                               # one past the last row
+    out = gpu_combine(bf16_dev(y), f32_dev(wts), i32_dev(dst))
+    exp = oracle.combine(y, wts, dst)
+    assert np.array_equal(bf16_host(out), exp)
+    assert np.all(exp[5] == 0)
+
+
+@pytest.mark.parametrize("K,fp8", [(3, False), (8, False), (8, True), (9, True)])
+def test_dispatch_skips_invalid_slots(oracle, K, fp8):
+    """A -1 or out-of-range slot is not written; every valid slot is."""
+    T, H = 30, 384
+    rng = np.random.default_rng(K * 3 + fp8)
+    x = wl.to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32))
+    perm = rng.permutation(T * K).astype(np.int32).reshape(T, K)
+    drop = rng.random((T, K)) < 0.25
+    drop[0, 0] = True
+    dst = perm.copy()
+    dst[drop] = -1
+    dst[0, 0] = T * K + 7                               # past the last row instead
+    dropped_rows, valid = perm[drop], perm[~drop]       # rows nobody / somebody writes
+    if fp8:
+        codes, scales = gpu_dispatch_fp8(bf16_dev(x), i32_dev(dst))
+        ec, es = oracle.dispatch_fp8(x, dst)
+        got = codes.view(torch.uint8).cpu().numpy()
+        assert np.array_equal(got[valid], ec[valid])
+        assert np.array_equal(scales.cpu().numpy()[valid].view(np.uint32), es[valid].view(np.uint32))
+        assert np.all(got[dropped_rows] == 0x7F)         # untouched poison
+    else:
+        got = bf16_host(gpu_dispatch_bf16(bf16_dev(x), i32_dev(dst)))
+        assert np.array_equal(got[valid], oracle.dispatch_bf16(x, dst)[valid])
+        assert np.all(got[dropped_rows] == 0xFFFF)
+
+
 # ------------------------------------------------------ the path end to end --
 
 @pytest.mark.parametrize("name", [n for n in ALL if "bf16" in wl.get(n).dispatch])

@@ -82,3 +82,21 @@ def test_regions_overflow_and_all_private(oracle, fp8):
     inp = wl.make_inputs(w)
     assert run_regions(oracle, inp, w.E, w.R, 2, 5, fp8) == 4       # bulk too small
     assert run_regions(oracle, inp, w.E, w.R, 1000, 0, fp8) == 0    # everything private
+
+
+@pytest.mark.parametrize("T,H,K,E,R,P,fp8", [
+    (9, 8, 2, 4, 1, 0, False),          # one 16-byte vector per row, one region
+    (17, 24, 5, 10, 5, 0, False),       # 3 vectors per row
+    (37, 1032, 3, 12, 4, 2, False),     # 129 vectors: a partial last group of 4 per thread
+    (50, 384, 8, 64, 64, 1, True),      # R = E, FP8
+    (300, 7168, 8, 256, 32, 3, True),
+])
+def test_regions_shapes(oracle, T, H, K, E, R, P, fp8):
+    import types
+    rng = np.random.default_rng(T + H)
+    ids = wl.routing_uniform(T, E, K, rng)
+    x = wl.to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32))
+    inp = types.SimpleNamespace(topk_ids=ids, tokens=x)
+    ref = oracle.layout(ids, E, R)
+    C = max(0, int(np.diff(ref.rank_offsets).max()) - P)
+    assert run_regions(oracle, inp, E, R, P, C, fp8) == 0
