@@ -55,13 +55,15 @@ def test_layout_full_size(oracle, name):
     assert_layout_equal(buf, ref, w.T, w.K, w.E, w.R)
 
 
-SHAPES = [  # T, K, E, R: fused single block, chunked, ragged tails, limits
+SHAPES = [  # T, K, E, R: single kernel, count/scan/rank, ragged tails, limits
     (0, 4, 16, 4), (1, 1, 1, 1), (1, 8, 256, 32), (3, 2, 4, 2), (33, 3, 7, 7),
     (1000, 6, 64, 8), (1024, 8, 256, 32), (1025, 8, 256, 32),
     (1500, 5, 40, 5), (4097, 2, 1024, 16), (5000, 8, 1024, 1024),
     (20000, 8, 384, 48), (70001, 4, 96, 12), (3000, 32, 64, 4),
     (300000, 1, 1, 1), (500, 8, 256, 32), (1365, 3, 5, 5), (3000, 3, 16, 4),
     (4096, 1, 1024, 2), (130000, 8, 128, 16),
+    # just above one kernel's size, T = 129 at K = 32, Qwen3-sized
+    (1025, 4, 16, 4), (129, 32, 64, 8), (16384, 8, 128, 16),
 ]
 
 

@@ -72,14 +72,26 @@ def _with_workspace(ids, E, R):
 def test_static_scratch_matches_workspace_layout_twice(lib):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
-    cases = [wl.get("prefill_kimi_k2"), wl.get("prefill_qwen3")]
-    for w in cases:                      # two calls in a row on the shared array
+    # large batches: count -> scan -> rank on the scratch array, one call
+    # after another, each reusing what the previous one left there
+    rng = np.random.default_rng(5)
+    big = [(32768, 8, 128, 16), (20000, 8, 384, 48)]
+    for T, K, E, R in big:
+        assert 0 < moe.moe_layout_workspace_bytes(T, K, E) <= SCRATCH_BYTES
+        ids = torch.from_numpy(wl.routing_uniform(T, E, K, rng)).cuda()
+        got = _static(lib, ids, E, R)
+        exp = _with_workspace(ids, E, R)
+        torch.cuda.synchronize()
+        for g, e in zip(got, exp):       # integer outputs: exact
+            assert torch.equal(g, e)
+    # the prefill workloads
+    for w in (wl.get("prefill_kimi_k2"), wl.get("prefill_qwen3")):
         assert 0 < moe.moe_layout_workspace_bytes(w.T, w.K, w.E) <= SCRATCH_BYTES
         ids = torch.from_numpy(wl.make_inputs(w).topk_ids).cuda()
         got = _static(lib, ids, w.E, w.R)
         exp = _with_workspace(ids, w.E, w.R)
         torch.cuda.synchronize()
-        for g, e in zip(got, exp):       # integer outputs: exact
+        for g, e in zip(got, exp):
             assert torch.equal(g, e)
     # a batch small enough to need no scratch goes through the same call
     w = wl.get("decode_dsv3")
