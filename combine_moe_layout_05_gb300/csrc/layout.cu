@@ -213,7 +213,7 @@ layout_rank_kernel(const int32_t *__restrict__ ids, int T, int K, int E, int R,
     }
     int lo, hi;
     warp_segment<kWarps>(m, w, lo, hi);
-    warp_count(mine, lo, hi, E, lane, rows + w * E);
+    warp_count<kSelf>(mine, lo, hi, E, lane, rows + w * E);
     __syncthreads();
 
     if (kSelf) {
@@ -241,7 +241,7 @@ layout_rank_kernel(const int32_t *__restrict__ ids, int T, int K, int E, int R,
         }
     }
     __syncthreads();
-    warp_rank(mine, lo, hi, E, K, first, lane, rows + w * E, dst_row, src_token);
+    warp_rank<kSelf>(mine, lo, hi, E, K, first, lane, rows + w * E, dst_row, src_token);
 }
 
 size_t rank_smem_bytes(const LayoutPlan &p, int T, int K, int E)

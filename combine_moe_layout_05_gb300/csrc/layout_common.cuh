@@ -64,16 +64,43 @@ __device__ __forceinline__ void warp_segment(int n, int w, int &lo, int &hi)
     hi = min(n, lo + seg);
 }
 
+// Bits that tell the ids 0 .. E-1 apart.
+__device__ __forceinline__ int id_bits(int E) { return 32 - __clz(E > 1 ? E - 1 : 1); }
+
+// The lanes of this warp whose valid id equals this lane's (0 for an invalid
+// id).  kBallot: from one ballot per id bit -- a lane stays in the set while
+// it agrees with this lane on every bit -- which measured faster in the
+// single-kernel layout; otherwise the warp match instruction, faster in the
+// ranking kernel of the multi-kernel layout.  Every lane of the warp must
+// call.
+template <bool kBallot>
+__device__ __forceinline__ unsigned match_ids(int id, bool ok, int bits, int lane)
+{
+    if (!kBallot) {
+        const unsigned m = __match_any_sync(kFullMask, ok ? id : -1 - lane);
+        return ok ? m : 0u;
+    }
+    unsigned m = __ballot_sync(kFullMask, ok);
+    for (int b = 0; b < bits; ++b) {
+        const bool set = (id >> b) & 1;
+        const unsigned v = __ballot_sync(kFullMask, set);
+        m &= set ? v : ~v;
+    }
+    return ok ? m : 0u;
+}
+
 // Adds the valid ids of ids[lo, hi) to this warp's private counter row:
-// one add per distinct id of each 32-entry batch (warp match).
+// one add per distinct id of each 32-entry batch.
+template <bool kBallot>
 __device__ __forceinline__ void warp_count(const int32_t *ids, int lo, int hi,
                                            int E, int lane, int32_t *row)
 {
+    const int bits = id_bits(E);
     for (int b = lo; b < hi; b += 32) {
         const int i = b + lane;
         const int id = i < hi ? ids[i] : -1;
         const bool ok = (unsigned)id < (unsigned)E;
-        const unsigned m = __match_any_sync(kFullMask, ok ? id : -1 - lane);
+        const unsigned m = match_ids<kBallot>(id, ok, bits, lane);
         if (ok && lane == 31 - __clz(m)) row[id] += __popc(m);
     }
 }
@@ -82,16 +109,18 @@ __device__ __forceinline__ void warp_count(const int32_t *ids, int lo, int hi,
 // counter of its id plus the number of lower lanes holding the same id;
 // the highest such lane then advances the counter.  Writes dst_row[first +
 // i] and src_token[slot]; an invalid id gets dst_row -1.
+template <bool kBallot>
 __device__ __forceinline__ void warp_rank(const int32_t *ids, int lo, int hi, int E,
                                           int K, int first, int lane, int32_t *row,
                                           int32_t *dst_row, int32_t *src_token)
 {
+    const int bits = id_bits(E);
     for (int b = lo; b < hi; b += 32) {
         const int i = b + lane;
         const bool valid = i < hi;
         const int id = valid ? ids[i] : -1;
         const bool ok = (unsigned)id < (unsigned)E;
-        const unsigned m = __match_any_sync(kFullMask, ok ? id : -1 - lane);
+        const unsigned m = match_ids<kBallot>(id, ok, bits, lane);
         if (ok) {
             const int slot = row[id] + __popc(m & ((1u << lane) - 1u));
             dst_row[first + i] = slot;
