@@ -40,7 +40,7 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kSelfMaxEntries = 4096;
-constexpr int kSelfChunk = 512;
+constexpr int kSelfChunk = 256;
 constexpr int kChunk = 1024;
 constexpr int kScanCells = 16 * 1024;    // chunks x E staged by the scan (64 KB)
 constexpr int kScanThreads = 1024;
