@@ -16,7 +16,7 @@
 // each token piece read once), but each of the K stores goes to the region
 // row of its slot.  recv: block = one packed row x a slice, 4 vectors of 16
 // bytes per thread; the row's rank is found by binary search of
-// rank_offsets.
+// rank_offsets, staged in shared memory first.
 #include "common.cuh"
 #include "internal.h"
 #include "moe_layout.h"
@@ -40,7 +40,7 @@ __device__ __forceinline__ bool region_of(int s, int e, int epr, const int32_t *
                                           uint8_t *bulk, float *bulk_sc, RegionDst &d)
 {
     const int r = e / epr;
-    const int i = s - __ldg(rank_offsets + r);
+    const int i = s - rank_offsets[r];
     if (i < P) {
         d = {priv, priv_sc, (size_t)r * P + i};
         return true;
@@ -52,7 +52,10 @@ __device__ __forceinline__ bool region_of(int s, int e, int epr, const int32_t *
     return false;
 }
 
-template <bool kFp8>
+// KT > 0: K known at compile time.  The row piece, the block's copy of
+// rank_offsets (shared memory) and a token's slots and experts are all
+// requested before the first store, so a block waits for memory once.
+template <int KT, bool kFp8>
 __global__ void __launch_bounds__(256)
 dispatch_send_kernel(const uint4 *__restrict__ tokens, int H, int K, int E, int epr,
                      const int32_t *__restrict__ ids, const int32_t *__restrict__ dst_row,
@@ -61,19 +64,14 @@ dispatch_send_kernel(const uint4 *__restrict__ tokens, int H, int K, int E, int 
                      uint8_t *__restrict__ bulk, float *__restrict__ bulk_sc,
                      uint32_t *__restrict__ dev_error)
 {
+    __shared__ int32_t s_ro[MOE_MAX_EXPERTS + 1];
     pdl_wait();
     pdl_trigger();
     const int t = blockIdx.x;
     const int u = blockIdx.y * blockDim.x + threadIdx.x;
     const int units = kFp8 ? (H >> 4) : (H >> 3);
     const bool active = u < units;
-    if (t == 0 && blockIdx.y == 0 && threadIdx.x == 0 && dev_error) {
-        uint32_t err = 0;
-        for (int r = 0; r < R; ++r)
-            if (__ldg(rank_offsets + r + 1) - __ldg(rank_offsets + r) - P > C)
-                err |= MOE_DEV_ERR_REGION_OVERFLOW;
-        *dev_error = err;
-    }
+    const int k_count = KT > 0 ? KT : K;
     const size_t vrow = (size_t)(H >> 3);
     uint4 a = make_uint4(0, 0, 0, 0), b = make_uint4(0, 0, 0, 0);
     if (active) {
@@ -84,6 +82,15 @@ dispatch_send_kernel(const uint4 *__restrict__ tokens, int H, int K, int E, int 
             a = ld_stream_v4(tokens + (size_t)t * vrow + u);
         }
     }
+    for (int q = threadIdx.x; q <= R; q += blockDim.x) s_ro[q] = __ldg(rank_offsets + q);
+    if (t == 0 && blockIdx.y == 0 && threadIdx.x == 0 && dev_error) {
+        uint32_t err = 0;
+        for (int r = 0; r < R; ++r)
+            if (__ldg(rank_offsets + r + 1) - __ldg(rank_offsets + r) - P > C)
+                err |= MOE_DEV_ERR_REGION_OVERFLOW;
+        *dev_error = err;
+    }
+    __syncthreads();
     Fp8Piece p;
     if (kFp8) {
         p = quantize16(a, b);        // every lane takes part (8-lane blocks)
@@ -93,14 +100,24 @@ dispatch_send_kernel(const uint4 *__restrict__ tokens, int H, int K, int E, int 
     }
     const size_t row_bytes = kFp8 ? (size_t)H : (size_t)H * 2;
     const int nb = H >> 7;
-    for (int k = 0; k < K; ++k) {
-        const int s = __ldg(dst_row + (size_t)t * K + k);
-        const int e = __ldg(ids + (size_t)t * K + k);
-        if ((unsigned)s >= (unsigned)rows || (unsigned)e >= (unsigned)E) continue;
-        RegionDst d;
-        if (!region_of(s, e, epr, rank_offsets, P, C, priv, priv_sc, bulk, bulk_sc, d)) continue;
-        st_v4(d.base + d.row * row_bytes + (size_t)u * 16, kFp8 ? p.codes : a);
-        if (kFp8 && (u & 7) == 0) d.scale_base[d.row * nb + (u >> 3)] = p.scale;
+    constexpr int G = KT > 0 && KT < 8 ? KT : 8;
+    for (int k0 = 0; k0 < k_count; k0 += G) {
+        int sl[G], ex[G];
+#pragma unroll
+        for (int j = 0; j < G; ++j) {
+            const bool in = KT > 0 || k0 + j < k_count;
+            sl[j] = in ? __ldg(dst_row + (size_t)t * k_count + k0 + j) : -1;
+            ex[j] = in ? __ldg(ids + (size_t)t * k_count + k0 + j) : -1;
+        }
+#pragma unroll
+        for (int j = 0; j < G; ++j) {
+            if ((unsigned)sl[j] >= (unsigned)rows || (unsigned)ex[j] >= (unsigned)E) continue;
+            RegionDst d;
+            if (!region_of(sl[j], ex[j], epr, s_ro, P, C, priv, priv_sc, bulk, bulk_sc, d))
+                continue;
+            st_v4(d.base + d.row * row_bytes + (size_t)u * 16, kFp8 ? p.codes : a);
+            if (kFp8 && (u & 7) == 0) d.scale_base[d.row * nb + (u >> 3)] = p.scale;
+        }
     }
 }
 
@@ -111,18 +128,22 @@ dispatch_recv_kernel(const uint8_t *__restrict__ priv, const float *__restrict__
                      const int32_t *__restrict__ rank_offsets, int R, int P, int C, int H,
                      uint8_t *__restrict__ packed, float *__restrict__ scales)
 {
+    __shared__ int32_t s_ro[MOE_MAX_EXPERTS + 1];
     pdl_wait();
     pdl_trigger();
+    // rank_offsets in shared memory: one parallel load, then the search
+    for (int q = threadIdx.x; q <= R; q += blockDim.x) s_ro[q] = __ldg(rank_offsets + q);
+    __syncthreads();
     const int row = blockIdx.x;
-    if (row >= __ldg(rank_offsets + R)) return;
+    if (row >= s_ro[R]) return;
     int lo = 0, hi = R;                 // largest r with rank_offsets[r] <= row
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
-        if (__ldg(rank_offsets + mid) <= row) lo = mid;
+        if (s_ro[mid] <= row) lo = mid;
         else hi = mid;
     }
     const int r = lo;
-    const int i = row - __ldg(rank_offsets + r);
+    const int i = row - s_ro[r];
     const uint8_t *src;
     const float *ssc;
     size_t srow;
@@ -159,6 +180,22 @@ dispatch_recv_kernel(const uint8_t *__restrict__ priv, const float *__restrict__
     }
 }
 
+template <int KT, bool kFp8>
+cudaError_t run_send(const void *tokens, int T, int H, int K, int E, int R,
+                     const int32_t *topk_ids, const int32_t *dst_row,
+                     const int32_t *rank_offsets, int P, void *priv, float *priv_scales,
+                     int C, void *bulk, float *bulk_scales, uint32_t *dev_error,
+                     cudaStream_t stream)
+{
+    const int units = kFp8 ? H / 16 : H / 8;
+    const int threads = pick_row_block(units);
+    const dim3 grid(T, ceil_div(units, threads));
+    return launch_pdl(dispatch_send_kernel<KT, kFp8>, grid, dim3(threads), 0, stream,
+                      static_cast<const uint4 *>(tokens), H, K, E, E / R, topk_ids, dst_row,
+                      rank_offsets, R, T * K, P, C, static_cast<uint8_t *>(priv), priv_scales,
+                      static_cast<uint8_t *>(bulk), bulk_scales, dev_error);
+}
+
 }  // namespace
 
 cudaError_t launch_dispatch_send(const void *tokens, int T, int H, int K, int E, int R,
@@ -167,18 +204,20 @@ cudaError_t launch_dispatch_send(const void *tokens, int T, int H, int K, int E,
                                  float *priv_scales, int C, void *bulk, float *bulk_scales,
                                  uint32_t *dev_error, cudaStream_t stream)
 {
-    const int units = fp8 ? H / 16 : H / 8;
-    const int threads = pick_row_block(units);
-    const dim3 grid(T, ceil_div(units, threads));
-    if (fp8)
-        return launch_pdl(dispatch_send_kernel<true>, grid, dim3(threads), 0, stream,
-                          static_cast<const uint4 *>(tokens), H, K, E, E / R, topk_ids, dst_row,
-                          rank_offsets, R, T * K, P, C, static_cast<uint8_t *>(priv), priv_scales,
-                          static_cast<uint8_t *>(bulk), bulk_scales, dev_error);
-    return launch_pdl(dispatch_send_kernel<false>, grid, dim3(threads), 0, stream,
-                      static_cast<const uint4 *>(tokens), H, K, E, E / R, topk_ids, dst_row,
-                      rank_offsets, R, T * K, P, C, static_cast<uint8_t *>(priv), priv_scales,
-                      static_cast<uint8_t *>(bulk), bulk_scales, dev_error);
+#define MOE_SEND_CASE(KV)                                                                     \
+    return fp8 ? run_send<KV, true>(tokens, T, H, K, E, R, topk_ids, dst_row, rank_offsets, P, \
+                                    priv, priv_scales, C, bulk, bulk_scales, dev_error, stream) \
+               : run_send<KV, false>(tokens, T, H, K, E, R, topk_ids, dst_row, rank_offsets, P,\
+                                     priv, priv_scales, C, bulk, bulk_scales, dev_error, stream)
+    switch (K) {
+    case 1: MOE_SEND_CASE(1);
+    case 2: MOE_SEND_CASE(2);
+    case 4: MOE_SEND_CASE(4);
+    case 6: MOE_SEND_CASE(6);
+    case 8: MOE_SEND_CASE(8);
+    default: MOE_SEND_CASE(0);
+    }
+#undef MOE_SEND_CASE
 }
 
 cudaError_t launch_dispatch_recv(const void *priv, const float *priv_scales, int P,

@@ -11,18 +11,24 @@ namespace moe {
 
 // Writes `x` (16 bytes at byte offset `off` of a packed row) to each slot in
 // slots[0 .. k_count); slots outside [0, rows) are skipped.  `slots` may
-// point to global or shared memory.  KT > 0 is a compile-time k_count.
+// point to global or shared memory or to registers.  KT > 0 is a
+// compile-time k_count.  All slots of a group of 8 are read before its first
+// store (a store is an ordering point for the compiler, so a slot read after
+// it would add one memory latency per slot).
 template <int KT>
 __device__ __forceinline__ void store_to_slots(const int32_t *slots, int k_count,
                                                int rows, uint8_t *packed,
                                                size_t row_bytes, size_t off,
                                                const uint4 &x)
 {
+    constexpr int G = KT > 0 && KT < 8 ? KT : 8;
+    for (int k0 = 0; k0 < k_count; k0 += G) {
+        int r[G];
 #pragma unroll
-    for (int k = 0; k < (KT > 0 ? KT : MOE_MAX_TOPK); ++k) {
-        if (KT == 0 && k >= k_count) break;
-        const int r = slots[k];
-        if ((unsigned)r < (unsigned)rows) st_v4(packed + (size_t)r * row_bytes + off, x);
+        for (int j = 0; j < G; ++j) r[j] = (KT > 0 || k0 + j < k_count) ? slots[k0 + j] : -1;
+#pragma unroll
+        for (int j = 0; j < G; ++j)
+            if ((unsigned)r[j] < (unsigned)rows) st_v4(packed + (size_t)r[j] * row_bytes + off, x);
     }
 }
 
@@ -80,7 +86,7 @@ __device__ __forceinline__ Fp8Piece quantize16(const uint4 &a, const uint4 &b)
 }
 
 // Writes a quantised piece (group g of 16 values) and, from the block's
-// first lane, its scale, to each slot.
+// first lane, its scale, to each slot (slots read as in store_to_slots).
 template <int KT>
 __device__ __forceinline__ void store_fp8_to_slots(const int32_t *slots, int k_count,
                                                    int rows, uint8_t *packed,
@@ -89,13 +95,17 @@ __device__ __forceinline__ void store_fp8_to_slots(const int32_t *slots, int k_c
 {
     const int nb = H >> 7;
     const bool leader = (g & 7) == 0;
+    constexpr int G = KT > 0 && KT < 8 ? KT : 8;
+    for (int k0 = 0; k0 < k_count; k0 += G) {
+        int r[G];
 #pragma unroll
-    for (int k = 0; k < (KT > 0 ? KT : MOE_MAX_TOPK); ++k) {
-        if (KT == 0 && k >= k_count) break;
-        const int r = slots[k];
-        if ((unsigned)r >= (unsigned)rows) continue;
-        st_v4(packed + (size_t)r * H + 16 * (size_t)g, p.codes);
-        if (leader) scales[(size_t)r * nb + (g >> 3)] = p.scale;
+        for (int j = 0; j < G; ++j) r[j] = (KT > 0 || k0 + j < k_count) ? slots[k0 + j] : -1;
+#pragma unroll
+        for (int j = 0; j < G; ++j) {
+            if ((unsigned)r[j] >= (unsigned)rows) continue;
+            st_v4(packed + (size_t)r[j] * H + 16 * (size_t)g, p.codes);
+            if (leader) scales[(size_t)r[j] * nb + (g >> 3)] = p.scale;
+        }
     }
 }
 
