@@ -19,7 +19,8 @@
 //    thread adds the warps' partial sums itself and holds the slots in
 //    registers; no histogram, no scan, no atomics;
 //  * the row slice is requested first, so its HBM latency overlaps the
-//    counting;
+//    counting; in the FP8 form it is quantised just before the block
+//    barrier, filling the time warps wait there;
 //  * slice 0 of each token writes its dst_row / src_token entries; block b
 //    also counts expert b (count and offset, and the rank offset when b
 //    starts a rank), and block 0 writes the error word.
@@ -147,6 +148,7 @@ layout_dispatch_kernel(const int32_t *__restrict__ ids, const uint4 *__restrict_
     // pass gives block b the count and offset of expert b
     // (offsets[e] = #{valid ids < e}), spreading those outputs over the grid.
     int sl[8];
+    Fp8Piece q0;                        // the first row piece, quantised before the barrier
     for (int k0 = 0; k0 < k_count; k0 += 8) {
         int tg[8];
 #pragma unroll
@@ -195,6 +197,7 @@ layout_dispatch_kernel(const int32_t *__restrict__ ids, const uint4 *__restrict_
             const uint32_t sum = __reduce_add_sync(kFullMask, v[j]);
             if (lane == 0) red[w][j] = sum;
         }
+        if (kFp8 && k0 == 0) q0 = quantize16(a, bv);   // fills the wait at the barrier
         __syncthreads();
         uint32_t tot[5] = {0, 0, 0, 0, 0};
 #pragma unroll
@@ -247,7 +250,7 @@ layout_dispatch_kernel(const int32_t *__restrict__ ids, const uint4 *__restrict_
         }
         const int32_t *slots = kRegSlots ? sl : slots_s;
         if (kFp8) {
-            const Fp8Piece p = quantize16(a, bv);   // every lane takes part
+            const Fp8Piece p = base == u0 ? q0 : quantize16(a, bv);   // every lane takes part
             if (active)
                 store_fp8_to_slots<KT>(slots, k_count, rows, packed, scales, H, u, p);
         } else if (active) {
