@@ -1,20 +1,25 @@
 #!/usr/bin/env python3
 """Benchmark of the single-GPU MoE layout + dispatch + combine path.
 
-One step = moe_layout -> moe_dispatch -> moe_combine on one batch of the
-workload (default: DeepSeek-V3-shaped decode, T=128 tokens, H=7168, E=256
-experts over R=32 regions, top-8, bf16 dispatch, per-expert-scalar stand-in
-experts whose outputs are materialised once before timing).  Prints one JSON
-line: whole-job tokens/s, per-kernel times and HBM GB/s, the roofline of the
-dominant kernel, an end-to-end figure through host buffers, clocks seen during
-the timed region, and the CPU oracle timed on the host.
+One step = moe_layout_dispatch (layout, then dispatch) -> moe_combine on one
+batch of the workload.  Default: the Qwen3-235B-shaped prefill (T=16384
+tokens, H=4096, E=128 experts over R=16 regions, top-8 Zipf(1.0) routing,
+1 % outlier rows) with block-scaled FP8 dispatch and bf16 combine; the
+stand-in experts (dequantised identity) are materialised once before timing.
+Prints one JSON line: whole-job tokens/s, per-call times and HBM GB/s, the
+roofline of the dominant call, an end-to-end figure through host buffers,
+clocks seen during the timed region, and the CPU oracle timed on the host.
+`--all` prints one such line per workload and dispatch variant.
 
-Timing: K steps are captured into CUDA graphs (the launch cost of a
-decode-sized step is comparable to its run time) and replayed between a
-barrier and a device synchronize; every step works on one of S rotating
-buffer sets whose total size is at least 3x the L2 cache, so each step starts
-cold in L2.  Per-kernel times come from event nodes recorded inside the same
-graphs.  `--impl reference` times the CPU oracle instead.
+Timing: the K steps of one pass are captured into CUDA graphs (the launch
+cost of a decode-sized step is comparable to its run time); the pass is
+replayed repeatedly, between a barrier and a device synchronize, until at
+least --min-seconds of device time have been measured, with CUDA events on
+the launching stream around every pass; ms_per_step is the median pass / K.
+Every step works on one of S rotating buffer sets whose total size is at
+least 3x the L2 cache, so each step starts cold in L2.  Each call of the step
+is also timed alone the same way.  `--impl reference` times the CPU oracle
+instead.
 
 Multi-GPU (torchrun): every rank runs its own replica on its own tokens (no
 data-path collective); the elapsed time is the maximum over ranks and the
@@ -42,23 +47,37 @@ METRIC = "dispatch+combine tokens/s and achieved HBM GB/s vs GB300 peak (1 GPU)"
 FALLBACK_HBM_GBS = 6800.0
 KERNELS = ("layout", "dispatch", "combine")
 
+# workload and dispatch variants of --all (the tiny workload is a parity case)
+ALL_VARIANTS = (("decode_dsv3", "bf16"), ("decode_dsv3_fp8", "fp8"),
+                ("prefill_kimi_k2", "bf16"), ("prefill_kimi_k2", "fp8"),
+                ("prefill_qwen3", "fp8"))
+
 
 # --------------------------------------------------------------- helpers --
 
 def parse_args(argv=None):
     p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=50000)
-    p.add_argument("--warmup", type=int, default=2000)
+    p.add_argument("--steps", type=int, default=200, help="steps per timed pass (K)")
+    p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    p.add_argument("--workload", default=None, help="workload name (default: decode_dsv3)")
+    p.add_argument("--workload", default=None, help="workload name (default: prefill_qwen3)")
     p.add_argument("--dispatch", choices=("bf16", "fp8"), default=None)
+    p.add_argument("--all", action="store_true",
+                   help="one line per workload and dispatch variant (%s)"
+                        % ", ".join(f"{n}/{d}" for n, d in ALL_VARIANTS))
+    p.add_argument("--min-seconds", type=float, default=1.0,
+                   help="device time over which K-step passes are repeated")
+    p.add_argument("--call-seconds", type=float, default=0.4,
+                   help="device time over which each call is timed alone")
     p.add_argument("--graph-steps", type=int, default=512,
                    help="steps per captured graph")
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="host time spent timing the oracle baseline")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-parity", action="store_true",
+                   help="skip the bench's own oracle check of one step")
     p.add_argument("--path", choices=("packed", "regions"), default="packed",
                    help="regions: dispatch through per-rank send regions (moe_dispatch_send, "
                         "private area of --private rows, bulk sized to the worst case) and "
@@ -151,41 +170,58 @@ def algorithmic_bytes(w, dispatch: str):
             "layout_dispatch": layout + disp - 4 * T * K}
 
 
-def kernel_source_hash(kernel: str) -> str:
-    srcs = {"layout": ["layout.cu", "layout_common.cuh"],
-            "dispatch": ["dispatch.cu", "rowops.cuh"],
-            "combine": ["combine.cu", "combine_common.cuh"],
-            "combine_fp8": ["combine_fp8.cu", "combine_common.cuh"],
-            "combine_rank_partial": ["combine_rank_partial.cu", "combine_common.cuh"],
-            "layout_dispatch": ["layout_dispatch.cu", "layout_common.cuh", "rowops.cuh",
-                                "layout.cu", "dispatch.cu"],
-            "dispatch_send": ["regions.cu", "rowops.cuh"],
-            "dispatch_recv": ["regions.cu"]}.get(kernel)
+# the sources each call's kernels are built from (their hash keys the DRAM
+# traffic rows in profiles/dram_traffic.json)
+CALL_SOURCES = {
+    "layout": ["layout.cu", "layout_common.cuh"],
+    "dispatch": ["dispatch.cu", "rowops.cuh"],
+    "combine": ["combine.cu", "combine_common.cuh"],
+    "combine_fp8": ["combine_fp8.cu", "combine_common.cuh"],
+    "combine_rank_partial": ["combine_rank_partial.cu", "combine_common.cuh"],
+    "layout_dispatch": ["layout_dispatch.cu", "layout_common.cuh", "rowops.cuh",
+                        "layout.cu", "dispatch.cu"],
+    "dispatch_send": ["regions.cu", "rowops.cuh"],
+    "dispatch_recv": ["regions.cu"],
+}
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
+
+
+def kernel_source_hash(kernel: str):
+    srcs = CALL_SOURCES.get(kernel)
     if srcs is None:
         return None
     h = hashlib.sha256()
     for f in srcs + ["common.cuh"]:
-        with open(os.path.join(ROOT, "combine_moe_layout_05_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        p = os.path.join(ROOT, "combine_moe_layout_05_gb300", "csrc", f)
+        if os.path.exists(p):
+            with open(p, "rb") as fh:
+                h.update(fh.read())
     return h.hexdigest()[:12]
 
 
-def profiled_traffic(kernel: str, workload: str, dispatch: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current source of that kernel; otherwise None."""
-    path = os.path.join(ROOT, "profiles", "dram_traffic.md")
-    if not os.path.exists(path):
+def profiled_traffic(kernel: str, workload: str, dispatch: str, path: str = TRAFFIC_FILE):
+    """DRAM bytes per launch from the committed ncu capture of this call, if
+    it was taken on the current source of that call; otherwise None."""
+    try:
+        with open(path) as f:
+            rows = json.load(f)["rows"]
+    except (OSError, ValueError, KeyError):
         return None
     want = kernel_source_hash(kernel)
-    for line in open(path):
-        cells = [c.strip() for c in line.strip().strip("|").split("|")]
-        if len(cells) >= 5 and cells[0] == kernel and cells[1] == workload \
-                and cells[2] == dispatch and cells[3] == want:
-            try:
-                return int(cells[4])
-            except ValueError:
-                return None
+    for r in rows:
+        if (r.get("call"), r.get("workload"), r.get("dispatch"), r.get("source_hash")) == \
+                (kernel, workload, dispatch, want):
+            return int(r["dram_bytes_per_launch"])
     return None
+
+
+def dtype_label(dispatch: str, combine: str) -> str:
+    d = ("fp8-e4m3 dispatch (1x128 fp32 block scales)" if dispatch == "fp8"
+         else "bf16 dispatch (bit copy)")
+    c = {"bf16": "bf16 combine, fp32 accumulate",
+         "fp8": "fp8-e4m3 combine input, fp32 accumulate",
+         "rank_partial": "bf16 combine, fp32 per-rank partials rounded to bf16"}[combine]
+    return f"{d}, {c}"
 
 
 class ClockSampler:
@@ -511,35 +547,182 @@ def time_oracle(w, dispatch, inp, y_bits, seconds: float, max_tokens=None, combi
             return T * n / el, T, n
 
 
-def graph_timer(torch, sets, n_sets, G, K):
-    """Returns time_ops(fn_step, n_steps) -> ms: captures fn over the rotating
-    sets into CUDA graphs of G steps (plus one of the remainder) and times
-    n_steps of them between CUDA events on the launching stream."""
-    def build(fn, n):
-        return capture(torch, lambda m, sh: [fn(sets[j % n_sets]) for j in range(m)], n)
+class StepGraphs:
+    """n_steps consecutive calls of fn(set j mod n_sets), captured into CUDA
+    graphs of G steps plus one graph of the remainder; replay() enqueues all
+    n_steps on the current stream."""
 
-    def time_ops(fn, n_steps, warmup):
-        g = build(fn, G)
+    def __init__(self, torch, body, n_steps, G):
+        self.torch = torch
+        self.g = capture(torch, body, G) if n_steps >= G else None
+        self.reps = n_steps // G
         rem = n_steps % G
-        gr = build(fn, rem) if rem else None
-        for _ in range(max(1, warmup // G)):
-            g.replay()
-        start = torch.cuda.Event(enable_timing=True)
-        stop = torch.cuda.Event(enable_timing=True)
+        self.gr = capture(torch, body, rem) if rem else None
+
+    def replay(self):
+        for _ in range(self.reps):
+            self.g.replay()
+        if self.gr is not None:
+            self.gr.replay()
+
+
+def timed_passes(torch, replay, min_seconds, min_passes=3, max_passes=100000):
+    """Replays one pass (replay()) until at least min_seconds of device time
+    are covered, with a CUDA event on the current stream between passes.
+    Returns the list of pass times in ms.  The caller synchronises and
+    brackets the call with barriers."""
+    s = torch.cuda.current_stream()
+    probe = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    probe[0].record(s)
+    replay()
+    probe[1].record(s)
+    probe[1].synchronize()
+    first = max(probe[0].elapsed_time(probe[1]), 1e-3)
+    n = int(min(max_passes, max(min_passes, math.ceil(1e3 * min_seconds / first))))
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+    ev[0].record(s)
+    for i in range(n):
+        replay()
+        ev[i + 1].record(s)
+    ev[n].synchronize()
+    return [ev[i].elapsed_time(ev[i + 1]) for i in range(n)]
+
+
+def measure_ours(args, w, dispatch, combine, rank, world, local, device, first_line=True):
+    """One bench line for workload w (dict), measured on this rank."""
+    import numpy as np
+    import torch
+    import combine_moe_layout_05_gb300 as moe
+
+    inp = wl_inputs(w, rank)
+    if combine == "fp8" and dispatch != "fp8":
+        raise SystemExit("--combine fp8 needs FP8 dispatch (--dispatch fp8)")
+    ops = step_ops(moe, dispatch, args.unfused, combine, args.path)
+    priv_rows = args.private if args.path == "regions" else None
+
+    # rotating buffer sets: total >= 3x L2, so every step starts cold in L2
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    first = BufferSet(w, dispatch, inp, None, device, priv_rows)
+    for _, fn in ops[:-1]:
+        fn(first)
+    torch.cuda.synchronize()
+    y_bits = expert_outputs(w, dispatch, inp, first) if combine != "fp8" else None
+    per_set = first.nbytes() + (0 if y_bits is None else y_bits.nbytes)
+    n_sets = max(2, math.ceil(3 * l2 / per_set))
+    del first
+    sets = [BufferSet(w, dispatch, inp, y_bits, device, priv_rows) for _ in range(n_sets)]
+    for b in sets:                       # eager pass: attributes, parity data
+        run_step(moe, b, dispatch, args.unfused, combine, args.path)
+    torch.cuda.synchronize()
+
+    K = args.steps
+    G = max(n_sets, (min(args.graph_steps, max(K, 1)) // n_sets) * n_sets)
+    step = lambda b: run_step(moe, b, dispatch, args.unfused, combine, args.path)
+    graphs = StepGraphs(torch, lambda m, sh: [step(sets[j % n_sets]) for j in range(m)], K, G)
+    for _ in range(max(1, math.ceil(args.warmup / max(K, 1)))):
+        graphs.replay()
+    torch.cuda.synchronize()
+    parity = None
+    if rank == 0 and not args.no_parity:
+        parity = check_parity(w, dispatch, inp, sets[(K - 1) % n_sets if K else 0], combine)
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    barrier(device)
+    torch.cuda.synchronize()
+    sampler.mark_start()
+    passes = timed_passes(torch, graphs.replay, args.min_seconds)
+    torch.cuda.synchronize()
+    sampler.mark_stop()
+    barrier(device)
+    time.sleep(0.15)
+    clocks = sampler.stop()
+    pass_ms = max_over_ranks(statistics.median(passes), device)
+    del graphs
+
+    # each call of the step alone: K launches over the same rotating sets
+    ab = algorithmic_bytes(w, dispatch)
+    peak, peak_src = read_peaks()
+    kernels = {}
+    for name, fn in ops:
+        cg = StepGraphs(torch, lambda m, sh, fn=fn: [fn(sets[j % n_sets]) for j in range(m)], K, G)
+        cg.replay()
         torch.cuda.synchronize()
-        start.record()
-        for _ in range(n_steps // G):
-            g.replay()
-        if gr is not None:
-            gr.replay()
-        stop.record()
-        torch.cuda.synchronize()
-        return start.elapsed_time(stop)
-    return time_ops
+        cp = timed_passes(torch, cg.replay, args.call_seconds)
+        us = 1e3 * max_over_ranks(statistics.median(cp), device) / K
+        kernels[name] = {"us": round(us, 3), "gbs": round(ab[name] / (us * 1e-6) / 1e9, 1),
+                         "bytes": ab[name], "passes": len(cp)}
+        del cg
+    dom = max(kernels, key=lambda k: kernels[k]["us"])
+    achieved = kernels[dom]["gbs"]
+
+    e2e = None
+    if not args.no_e2e:
+        drv = Driver()
+        try:
+            e2e = run_e2e(args, w, dispatch, combine, inp, sets, n_sets, G, device, torch, moe, drv)
+        finally:
+            drv.close()
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline and world == 1:
+        tps, tsamp, nst = time_oracle(w, dispatch, inp, y_bits, args.cpu_seconds, combine=combine)
+        cpu = {"value": round(tps, 1), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+               **host_info(),
+               "sample": f"{nst} oracle steps (layout + {dispatch} dispatch + {combine} combine) "
+                         f"of the full {w.name} batch (T={tsamp}), single thread, "
+                         f"{args.cpu_seconds:.0f} s budget"}
+
+    value = world * w.T * K / (pass_ms * 1e-3)
+    lps = launches_per_step(w, dispatch, args.unfused, args.path)
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s",
+        "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": round(pass_ms / K, 6), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": dtype_label(dispatch, combine),
+        "data": "synthetic",
+        "timing": {"passes": len(passes), "steps_per_pass": K,
+                   "pass_ms_median": round(statistics.median(passes), 4),
+                   "pass_ms_min": round(min(passes), 4), "pass_ms_max": round(max(passes), 4),
+                   "device_seconds": round(sum(passes) / 1e3, 3),
+                   "method": "K-step pass replayed until >= %.1f s of device time; CUDA "
+                             "events on the launching stream between passes; median pass "
+                             "(max over ranks) / K" % args.min_seconds},
+        "config": {"workload": w.name, "T": w.T, "H": w.H, "E": w.E, "R": w.R,
+                   "K": w.K, "dispatch": dispatch,
+                   "combine": {"fp8": "e4m3 + block scales in (identity experts), f32 accumulate",
+                               "rank_partial": "bf16 in, per-rank f32 partials rounded to bf16, "
+                                               "f32 sum over ranks",
+                               "bf16": "bf16 in, f32 accumulate"}[combine],
+                   "experts": w.experts, "routing": w.routing,
+                   "calls": [n for n, _ in ops], "path": args.path,
+                   "l2": f"{n_sets} rotating buffer sets, {n_sets * per_set / 1e6:.0f} MB "
+                         f"> 3x L2 ({l2 / 1e6:.0f} MB); every step cold in L2",
+                   "launch": f"CUDA graphs of {G} steps, programmatic dependent launch",
+                   "kernel_timing": "each call alone: K launches in CUDA graphs over the "
+                                    "same rotating sets, passes repeated, median pass",
+                   "parallelism": f"replicas x{world}"},
+        "kernels": kernels,
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "peak_source": peak_src,
+                     "traffic": profiled_traffic(dom, w.name, dispatch)},
+        "e2e": e2e, "gpu_launches": lps * K * len(passes), "launches_per_step": lps,
+        "clocks": clocks, "cpu_baseline": cpu, "parity": parity,
+    }
+    del sets
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return line
+
+
+def wl_inputs(w, rank):
+    from combine_moe_layout_05_gb300 import workload as wl
+    return wl.make_inputs(w, seed=shard_seed(w.seed, rank))
 
 
 def run_ours(args):
-    import numpy as np
     import torch
     import combine_moe_layout_05_gb300 as moe
     from combine_moe_layout_05_gb300 import build as moe_build
@@ -557,121 +740,16 @@ def run_ours(args):
     moe_build.build()
     moe.load()
 
-    w = wl.get(args.workload or wl.HEADLINE)
-    dispatch = args.dispatch or w.dispatch[0]
-    inp = wl.make_inputs(w, seed=shard_seed(w.seed, rank))
-    if args.combine == "fp8" and dispatch != "fp8":
-        raise SystemExit("--combine fp8 needs FP8 dispatch (--dispatch fp8)")
-    ops = step_ops(moe, dispatch, args.unfused, args.combine, args.path)
-    priv_rows = args.private if args.path == "regions" else None
-
-    # rotating buffer sets: total >= 3x L2, so every step starts cold in L2
-    l2 = torch.cuda.get_device_properties(device).L2_cache_size
-    first = BufferSet(w, dispatch, inp, None, device, priv_rows)
-    for _, fn in ops[:-1]:
-        fn(first)
-    torch.cuda.synchronize()
-    y_bits = expert_outputs(w, dispatch, inp, first) if args.combine != "fp8" else None
-    per_set = first.nbytes() + (0 if y_bits is None else y_bits.nbytes)
-    n_sets = max(2, math.ceil(3 * l2 / per_set))
-    sets = [BufferSet(w, dispatch, inp, y_bits, device, priv_rows) for _ in range(n_sets)]
-    del first
-    for b in sets:                       # eager pass: attributes, parity data
-        run_step(moe, b, dispatch, args.unfused, args.combine, args.path)
-    torch.cuda.synchronize()
-
-    K = args.steps
-    G = max(n_sets, (min(args.graph_steps, max(K, 1)) // n_sets) * n_sets)
-    step = lambda b: run_step(moe, b, dispatch, args.unfused, args.combine, args.path)
-    g = capture(torch, lambda m, sh: [step(sets[j % n_sets]) for j in range(m)], G)
-    rem = K % G
-    gr = capture(torch, lambda m, sh: [step(sets[j % n_sets]) for j in range(m)], rem) if rem else None
-    for _ in range(max(1, args.warmup // G)):
-        g.replay()
-    for j in range(args.warmup % G):
-        step(sets[j % n_sets])
-    torch.cuda.synchronize()
-    parity = check_parity(w, dispatch, inp, sets[-1], args.combine) if rank == 0 else None
-
-    sampler = ClockSampler(local)
-    sampler.start()
-    time.sleep(0.3)
-    start = torch.cuda.Event(enable_timing=True)
-    stop = torch.cuda.Event(enable_timing=True)
-    barrier(device)
-    torch.cuda.synchronize()
-    sampler.mark_start()
-    start.record()
-    for _ in range(K // G):
-        g.replay()
-    if gr is not None:
-        gr.replay()
-    stop.record()
-    torch.cuda.synchronize()
-    sampler.mark_stop()
-    barrier(device)
-    time.sleep(0.15)
-    clocks = sampler.stop()
-    elapsed_ms = max_over_ranks(start.elapsed_time(stop), device)
-
-    # each call of the step alone: K launches over the same rotating sets
-    time_ops = graph_timer(torch, sets, n_sets, G, K)
-    ab = algorithmic_bytes(w, dispatch)
-    peak, peak_src = read_peaks()
-    kernels = {}
-    for name, fn in ops:
-        ms = time_ops(fn, K, args.warmup)
-        us = 1e3 * ms / K
-        kernels[name] = {"us": round(us, 3), "gbs": round(ab[name] / (us * 1e-6) / 1e9, 1),
-                         "bytes": ab[name]}
-    dom = max(kernels, key=lambda k: kernels[k]["us"])
-    achieved = kernels[dom]["gbs"]
-
-    drv = Driver()
-    e2e = None
-    if not args.no_e2e:
-        e2e = run_e2e(args, w, dispatch, inp, sets, n_sets, device, torch, moe, drv)
-    drv.close()
-
-    cpu = None
-    if rank == 0 and not args.no_cpu_baseline and world == 1:
-        tps, tsamp, nst = time_oracle(w, dispatch, inp, y_bits, args.cpu_seconds, combine=args.combine)
-        cpu = {"value": round(tps, 1), "unit": "tokens/s", "cores": 1, "kind": "oracle",
-               **host_info(),
-               "sample": f"{nst} oracle steps of the full {w.name} batch "
-                         f"(T={tsamp}), single thread, {args.cpu_seconds:.0f} s budget"}
-
-    value = world * w.T * K / (elapsed_ms * 1e-3)
-    line = {
-        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s",
-        "n_gpus": world, "steps": K, "warmup": args.warmup,
-        "ms_per_step": round(elapsed_ms / K, 6), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic",
-        "config": {"workload": w.name, "T": w.T, "H": w.H, "E": w.E, "R": w.R,
-                   "K": w.K, "dispatch": dispatch,
-                   "combine": {"fp8": "e4m3 + block scales in (identity experts), f32 accumulate",
-                               "rank_partial": "bf16 in, per-rank f32 partials rounded to bf16, "
-                                               "f32 sum over ranks",
-                               "bf16": "bf16 in, f32 accumulate"}[args.combine],
-                   "experts": w.experts, "routing": w.routing,
-                   "calls": [n for n, _ in ops], "path": args.path,
-                   "l2": f"{n_sets} rotating buffer sets, {n_sets * per_set / 1e6:.0f} MB "
-                         f"> 3x L2 ({l2 / 1e6:.0f} MB); every step cold in L2",
-                   "launch": f"CUDA graphs of {G} steps, programmatic dependent launch",
-                   "kernel_timing": "each call alone: K launches in CUDA graphs over the "
-                                    "same rotating sets, CUDA events around the replays",
-                   "parallelism": f"replicas x{world}"},
-        "kernels": kernels,
-        "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
-                     "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "peak_source": peak_src,
-                     "traffic": profiled_traffic(dom, w.name, dispatch)},
-        "e2e": e2e, "gpu_launches": launches_per_step(w, dispatch, args.unfused, args.path) * K,
-        "clocks": clocks, "cpu_baseline": cpu, "parity": parity,
-    }
-    if rank == 0:
-        print(json.dumps(line), flush=True)
+    if args.all:
+        variants = list(ALL_VARIANTS)
+    else:
+        name = args.workload or wl.HEADLINE
+        w = wl.get(name)
+        variants = [(name, args.dispatch or w.dispatch[0])]
+    for name, dispatch in variants:
+        line = measure_ours(args, wl.get(name), dispatch, args.combine, rank, world, local, device)
+        if rank == 0:
+            print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
@@ -688,16 +766,16 @@ def launches_per_step(w, dispatch, unfused, path="packed") -> int:
     return moe.moe_layout_dispatch_kernels(w.T, w.H, w.K, w.E, dispatch == "fp8") + 1
 
 
-def run_e2e(args, w, dispatch, inp, sets, n_sets, device, torch, moe, drv):
+def run_e2e(args, w, dispatch, combine, inp, sets, n_sets, G, device, torch, moe, drv):
     """The same steps through host buffers, as a serving loop runs them: each
     step copies its tokens, ids and weights (one contiguous buffer) from
-    page-locked host memory,
-    runs the calls, and copies its output back to page-locked host memory,
-    all inside the timed region.  Copies and compute sit on three streams
-    (host-to-device, compute, device-to-host) so step j+1's upload and step
-    j-1's download overlap step j's kernels; events order each buffer set's
-    reuse (an upload waits for the compute that last read the set, a compute
-    waits for the download that last read its output)."""
+    page-locked host memory, runs the calls, and copies its output back to
+    page-locked host memory, all inside the timed region.  Copies and compute
+    sit on three streams (host-to-device, compute, device-to-host) so step
+    j+1's upload and step j-1's download overlap step j's kernels; events
+    order each buffer set's reuse (an upload waits for the compute that last
+    read the set, a compute waits for the download that last read its
+    output).  Passes of K steps are repeated like the device-resident run."""
     import numpy as np
     packed_in = pack_inputs(w, inp)
     h2d = packed_in.nbytes
@@ -725,7 +803,7 @@ def run_e2e(args, w, dispatch, inp, sets, n_sets, device, torch, moe, drv):
             comp.wait_event(up_done)
             if j - n_sets in down_done:       # the set's previous output was read
                 comp.wait_event(down_done[j - n_sets])
-            run_step(moe, b, dispatch, args.unfused, args.combine, args.path)
+            run_step(moe, b, dispatch, args.unfused, combine, args.path)
             comp_done[j] = torch.cuda.Event()
             comp_done[j].record(comp)
             with torch.cuda.stream(down):
@@ -737,37 +815,53 @@ def run_e2e(args, w, dispatch, inp, sets, n_sets, device, torch, moe, drv):
         comp.wait_stream(down)
 
     K = args.steps
-    G = max(n_sets, (min(args.graph_steps, max(K, 1)) // n_sets) * n_sets)
     torch.cuda.synchronize()
-    g = capture(torch, body, G)
-    rem = K % G
-    gr = capture(torch, body, rem) if rem else None
-    for _ in range(max(1, args.warmup // G)):
-        g.replay()
-    start = torch.cuda.Event(enable_timing=True)
-    stop = torch.cuda.Event(enable_timing=True)
-    barrier(device)
-    torch.cuda.synchronize()
-    start.record()
-    for _ in range(K // G):
-        g.replay()
-    if gr is not None:
-        gr.replay()
-    stop.record()
+    graphs = StepGraphs(torch, body, K, G)
+    graphs.replay()
     torch.cuda.synchronize()
     barrier(device)
-    ms = max_over_ranks(start.elapsed_time(stop), device)
+    torch.cuda.synchronize()
+    passes = timed_passes(torch, graphs.replay, args.min_seconds / 2)
+    torch.cuda.synchronize()
+    barrier(device)
+    ms = max_over_ranks(statistics.median(passes), device)
     _, world, _ = dist_env()
     # the copies brought back the same result the device-resident steps made
     out0 = np.ctypeslib.as_array((ctypes.c_uint8 * d2h).from_address(host[0]["out"]))
     same = np.array_equal(out0, sets[0].out.view(torch.uint8).cpu().numpy().ravel())
+    del graphs
     return {"value": round(world * w.T * K / (ms * 1e-3), 1), "unit": "tokens/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "ms_per_step": round(ms / K, 6), "output_matches_device_run": bool(same),
+            "ms_per_step": round(ms / K, 6), "passes": len(passes),
+            "output_matches_device_run": bool(same),
             "pipeline": "H2D, compute and D2H on three streams, overlapping across steps"}
 
 
 # ------------------------------------------------------- reference (oracle) --
+
+def host_expert_outputs(w, dispatch, inp, dst_row, expert_offsets):
+    """The stand-in experts' outputs computed on the host (reference arm)."""
+    import numpy as np
+    import torch
+    import oracle
+    from combine_moe_layout_05_gb300 import experts as ex
+    from combine_moe_layout_05_gb300 import workload as wl
+    if w.experts == "random" or (dispatch == "fp8" and w.experts == "scale"):
+        return wl.random_rows(w.T * w.K, w.H, inp.expert_rows_seed)
+    if dispatch == "fp8":
+        codes, scales = oracle.dispatch_fp8(inp.tokens, dst_row)
+        y = ex.dequant_rows(torch.from_numpy(codes).view(torch.float8_e4m3fn),
+                            torch.from_numpy(scales))
+    else:
+        packed = torch.from_numpy(oracle.dispatch_bf16(inp.tokens, dst_row).view(np.int16))
+        packed = packed.view(torch.bfloat16)
+        if w.experts == "scale":
+            y = ex.scale_rows(packed, torch.from_numpy(expert_offsets),
+                              torch.from_numpy(inp.expert_scale))
+        else:
+            y = packed
+    return y.view(torch.int16).numpy().view(np.uint16)
+
 
 def run_reference(args):
     rank, world, _ = dist_env()
@@ -780,12 +874,8 @@ def run_reference(args):
     dispatch = args.dispatch or w.dispatch[0]
     inp = wl.make_inputs(w)
     ref = oracle.layout(inp.topk_ids, w.E, w.R)
-    if args.combine == "fp8":
-        y_bits = None
-    elif dispatch == "bf16":
-        y_bits = oracle.dispatch_bf16(inp.tokens, ref.dst_row)
-    else:
-        y_bits = wl.random_rows(w.T * w.K, w.H, inp.expert_rows_seed)
+    y_bits = None if args.combine == "fp8" else host_expert_outputs(
+        w, dispatch, inp, ref.dst_row, ref.expert_offsets)
     # size each step so the whole run stays within about 90 s of host time
     t0 = time.perf_counter()
     time_oracle(w, dispatch, inp, y_bits, 0.0, combine=args.combine)
@@ -799,13 +889,14 @@ def run_reference(args):
         time_oracle(w, dispatch, inp, y_bits, 0.0, max_tokens=T_s, combine=args.combine)
     el = time.perf_counter() - t0
     value = T_s * args.steps / el
-    sample = (f"each step: oracle layout + {dispatch} dispatch + combine on the first "
-              f"{T_s} of the {w.T} tokens of {w.name}, single thread")
+    sample = (f"each step: oracle layout + {dispatch} dispatch + {args.combine} combine on "
+              f"the first {T_s} of the {w.T} tokens of {w.name}, single thread")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(1e3 * el / args.steps, 6), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": dtype_label(dispatch, args.combine),
+        "data": "synthetic",
         "config": {"workload": w.name, "T": w.T, "H": w.H, "E": w.E, "R": w.R, "K": w.K,
                    "dispatch": dispatch, "sample_tokens_per_step": T_s},
         "cpu_baseline": {"value": round(value, 1), "unit": "tokens/s", "cores": 1,

@@ -7,6 +7,7 @@ binds it with ctypes.  ``workload`` draws seeded synthetic routing inputs and
 dispatch and combine.
 """
 from ._binding import (MOE_DEV_ERR_DUPLICATE, MOE_DEV_ERR_EXPERT_RANGE,
+                       MOE_DEV_ERR_REGION_OVERFLOW,
                        LayoutBuffers, MoeError, declared_functions,
                        library_path, load, moe_combine, moe_combine_fp8,
                        moe_combine_rank_partial,
@@ -17,7 +18,8 @@ from ._binding import (MOE_DEV_ERR_DUPLICATE, MOE_DEV_ERR_EXPERT_RANGE,
                        moe_status_string)
 
 __all__ = [
-    "MOE_DEV_ERR_DUPLICATE", "MOE_DEV_ERR_EXPERT_RANGE", "LayoutBuffers",
+    "MOE_DEV_ERR_DUPLICATE", "MOE_DEV_ERR_EXPERT_RANGE", "MOE_DEV_ERR_REGION_OVERFLOW",
+    "LayoutBuffers",
     "MoeError", "declared_functions", "library_path", "load", "moe_combine",
     "moe_combine_fp8", "moe_combine_rank_partial",
     "moe_dispatch", "moe_dispatch_recv", "moe_dispatch_send", "moe_layout", "moe_layout_dispatch", "moe_layout_dispatch_kernels", "moe_layout_static",

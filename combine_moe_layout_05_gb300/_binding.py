@@ -19,6 +19,7 @@ from . import build as _build
 MOE_OK = 0
 MOE_DEV_ERR_EXPERT_RANGE = 1
 MOE_DEV_ERR_DUPLICATE = 2
+MOE_DEV_ERR_REGION_OVERFLOW = 4
 
 _lock = threading.Lock()
 _lib = None

@@ -144,6 +144,7 @@ dispatch_recv_kernel(const uint8_t *__restrict__ priv, const float *__restrict__
     }
     const int r = lo;
     const int i = row - s_ro[r];
+    if (i < 0) return;                  // row below rank_offsets[0]: no region row
     const uint8_t *src;
     const float *ssc;
     size_t srow;

@@ -250,6 +250,9 @@ MOE_API moe_status_t moe_combine_rank_partial(const void *expert_out,
  *        16-byte aligned.  priv_scales [R, P, H/128], bulk_scales [R, C, H/128]
  *        fp32 (fp8 == 1 only).  P >= 0, C >= 0.
  * topk_ids, dst_row [T, K] int32 and rank_offsets [R+1] int32 from moe_layout.
+ *        rank_offsets must be moe_layout's output (non-decreasing, starting at
+ *        0); moe_dispatch_recv skips packed rows outside
+ *        [rank_offsets[0], rank_offsets[R]).
  * dev_error (send; may be NULL) is overwritten with
  *        MOE_DEV_ERR_REGION_OVERFLOW when some n_r exceeds P + C, else 0.
  * H % 8 == 0 (H % 128 == 0 for fp8), E % R == 0.  T == 0 is a no-op.
@@ -321,7 +324,10 @@ MOE_API int32_t moe_layout_dispatch_kernels(int32_t T, int32_t H, int32_t K,
  *   batches above about 12.5 million entries are rejected.
  * - Set-up: the first call on a device looks up the array's device address
  *   (cudaGetSymbolAddress, with that device current); make that first call
- *   before any stream capture.  Set-up failure returns MOE_ERR_CUDA.
+ *   before any stream capture.  Set-up failure returns MOE_ERR_CUDA.  The
+ *   address is kept for the life of the process: after cudaDeviceReset on a
+ *   device the kept address is stale, so do not call moe_layout_static on
+ *   that device again in the same process.
  * - Sharing: all calls on a device share the one array, and it keeps the last
  *   call's contents.  Nothing in it needs to start at zero: each call writes
  *   every scratch entry before reading it.  Calls that can run at the same

@@ -177,3 +177,14 @@ def test_missing_library_fails_loudly(tmp_path):
     r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True,
                        timeout=120)
     assert r.returncode == 0, r.stderr + r.stdout
+
+
+def test_error_bits_agree_between_header_and_binding():
+    import re
+    text = open(os.path.join(ROOT, "include", "moe_layout.h")).read()
+    bits = {m.group(1): int(m.group(2))
+            for m in re.finditer(r"#define (MOE_DEV_ERR_\w+)\s+(\d+)u", text)}
+    assert bits == {"MOE_DEV_ERR_EXPERT_RANGE": 1, "MOE_DEV_ERR_DUPLICATE": 2,
+                    "MOE_DEV_ERR_REGION_OVERFLOW": 4}
+    for name, v in bits.items():
+        assert getattr(moe, name) == v, name

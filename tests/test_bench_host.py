@@ -79,6 +79,37 @@ def test_algorithmic_bytes_decode():
     assert f["dispatch"] == 128 * 7168 * 2 + 128 * 8 * (7168 + 4 * 56) + 128 * 8 * 4
 
 
+def test_traffic_rows_keyed_by_source_hash(tmp_path):
+    h = bench.kernel_source_hash("combine")
+    f = tmp_path / "t.json"
+    f.write_text(json.dumps({"rows": [
+        {"call": "combine", "workload": "decode_dsv3", "dispatch": "bf16",
+         "source_hash": h, "dram_bytes_per_launch": 123},
+        {"call": "combine", "workload": "prefill_qwen3", "dispatch": "fp8",
+         "source_hash": "000000000000", "dram_bytes_per_launch": 456}]}))
+    assert bench.profiled_traffic("combine", "decode_dsv3", "bf16", str(f)) == 123
+    assert bench.profiled_traffic("combine", "prefill_qwen3", "fp8", str(f)) is None  # stale
+    assert bench.profiled_traffic("combine", "tiny", "bf16", str(f)) is None
+    assert bench.profiled_traffic("combine", "decode_dsv3", "bf16", str(tmp_path / "x")) is None
+
+
+def test_committed_traffic_file_parses():
+    with open(bench.TRAFFIC_FILE) as f:
+        rows = json.load(f)["rows"]
+    for r in rows:
+        assert r["call"] in bench.CALL_SOURCES
+        assert r["dram_bytes_per_launch"] > 0 and len(r["source_hash"]) == 12
+
+
+def test_default_workload_is_the_largest_config():
+    args = bench.parse_args([])
+    assert args.workload is None and wl.HEADLINE == "prefill_qwen3"
+    w = wl.get(wl.HEADLINE)
+    assert w.dispatch[0] == "fp8" and args.combine == "bf16"
+    assert all(w.T * w.H >= v.T * v.H for v in wl.WORKLOADS.values())
+    assert bench.dtype_label("fp8", "bf16").startswith("fp8-e4m3 dispatch")
+
+
 def test_reference_arm_runs_on_cpu():
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
                         "--workload", "tiny", "--steps", "3", "--warmup", "1"],

@@ -33,11 +33,13 @@ def test_bench_line(args):
     d = _bench(*args)
     for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
                 "higher_is_better", "scaling", "dtype", "data", "config", "roofline",
-                "gpu_launches", "clocks"):
+                "gpu_launches", "clocks", "timing"):
         assert key in d, key
+    t = d["timing"]
+    assert t["passes"] >= 3 and t["steps_per_pass"] == 64
+    assert d["gpu_launches"] == d["launches_per_step"] * 64 * t["passes"]
     assert d["parity"] == "bit-exact"
     assert d["value"] > 0 and d["steps"] == 64 and d["n_gpus"] == 1
-    assert d["gpu_launches"] >= 2 * 64
     assert d["config"]["workload"] == "tiny"
     r = d["roofline"]
     assert r["bound"] == "hbm" and r["achieved"] > 0 and r["peak"] > 0
