@@ -179,7 +179,7 @@ CALL_SOURCES = {
     "combine_fp8": ["combine_fp8.cu", "combine_common.cuh"],
     "combine_rank_partial": ["combine_rank_partial.cu", "combine_common.cuh"],
     "layout_dispatch": ["layout_dispatch.cu", "layout_common.cuh", "rowops.cuh",
-                        "layout.cu", "dispatch.cu"],
+                        "layout.cu", "dispatch.cu", "layout_dispatch_prefill.cu"],
     "dispatch_send": ["regions.cu", "rowops.cuh"],
     "dispatch_recv": ["regions.cu"],
 }

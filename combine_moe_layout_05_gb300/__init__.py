@@ -7,7 +7,7 @@ binds it with ctypes.  ``workload`` draws seeded synthetic routing inputs and
 dispatch and combine.
 """
 from ._binding import (MOE_DEV_ERR_DUPLICATE, MOE_DEV_ERR_EXPERT_RANGE,
-                       MOE_DEV_ERR_REGION_OVERFLOW,
+                       MOE_DEV_ERR_REGION_OVERFLOW, MOE_DEV_ERR_TIMEOUT,
                        LayoutBuffers, MoeError, declared_functions,
                        library_path, load, moe_combine, moe_combine_fp8,
                        moe_combine_rank_partial,
@@ -19,6 +19,7 @@ from ._binding import (MOE_DEV_ERR_DUPLICATE, MOE_DEV_ERR_EXPERT_RANGE,
 
 __all__ = [
     "MOE_DEV_ERR_DUPLICATE", "MOE_DEV_ERR_EXPERT_RANGE", "MOE_DEV_ERR_REGION_OVERFLOW",
+    "MOE_DEV_ERR_TIMEOUT",
     "LayoutBuffers",
     "MoeError", "declared_functions", "library_path", "load", "moe_combine",
     "moe_combine_fp8", "moe_combine_rank_partial",

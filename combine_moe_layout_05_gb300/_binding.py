@@ -20,6 +20,7 @@ MOE_OK = 0
 MOE_DEV_ERR_EXPERT_RANGE = 1
 MOE_DEV_ERR_DUPLICATE = 2
 MOE_DEV_ERR_REGION_OVERFLOW = 4
+MOE_DEV_ERR_TIMEOUT = 8
 
 _lock = threading.Lock()
 _lib = None

@@ -80,22 +80,28 @@ __host__ __device__ constexpr int ceil_div(int a, int b) { return (a + b - 1) / 
 __host__ __device__ constexpr int align4(int n) { return (n + 3) & ~3; }
 
 // Copies n int32 values from global to shared memory with asynchronous
-// copies issued by all threads of the block (every request is in flight at
-// once, so the block pays one memory latency, not one per loop trip).  The
-// caller must call cp_async_wait_all() and then __syncthreads().
-__device__ __forceinline__ void stage_i32(int32_t *dst, const int32_t *src, int n)
+// copies issued by all threads of the block, or by the `nthreads` threads
+// numbered `tid` = 0 .. nthreads-1 (every request is in flight at once, so
+// the block pays one memory latency, not one per loop trip).  The caller
+// must call cp_async_wait_all() and then synchronise those threads.
+__device__ __forceinline__ void stage_i32(int32_t *dst, const int32_t *src, int n,
+                                          int tid = -1, int nthreads = 0)
 {
+    if (tid < 0) {
+        tid = threadIdx.x;
+        nthreads = blockDim.x;
+    }
     const unsigned base = (unsigned)__cvta_generic_to_shared(dst);
     const bool vec = ((reinterpret_cast<uintptr_t>(src) | base) & 15) == 0;
     int done = 0;
     if (vec) {
         const int n4 = n >> 2;
-        for (int i = threadIdx.x; i < n4; i += blockDim.x)
+        for (int i = tid; i < n4; i += nthreads)
             asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
                          :: "r"(base + 16u * i), "l"(src + 4 * i) : "memory");
         done = n4 << 2;
     }
-    for (int i = done + threadIdx.x; i < n; i += blockDim.x)
+    for (int i = done + tid; i < n; i += nthreads)
         asm volatile("cp.async.ca.shared.global [%0], [%1], 4;"
                      :: "r"(base + 4u * i), "l"(src + i) : "memory");
     asm volatile("cp.async.commit_group;" ::: "memory");

@@ -20,6 +20,12 @@ LayoutPlan plan_layout(int T, int K, int E);
 bool layout_supported(int T, int K, int E);
 size_t layout_workspace_bytes(const LayoutPlan &plan, int E);
 
+// The counting kernel of the multi-launch layout alone: chunk histograms to
+// ws_cnt[chunks][E], chunk error bits to ws_err[chunks], dev_error zeroed.
+cudaError_t launch_layout_count(const int32_t *topk_ids, int T, int K, int E,
+                                const LayoutPlan &plan, int32_t *ws_cnt, uint32_t *ws_err,
+                                uint32_t *dev_error, cudaStream_t stream);
+
 cudaError_t launch_layout(const int32_t *topk_ids, int T, int K, int E, int R,
                           int32_t *expert_counts, int32_t *expert_offsets,
                           int32_t *rank_offsets, int32_t *src_token,
@@ -68,6 +74,30 @@ cudaError_t launch_layout_dispatch(const int32_t *topk_ids, const void *tokens,
                                    int32_t *dst_row, uint32_t *dev_error,
                                    void *packed, float *scales, void *workspace,
                                    cudaStream_t stream);
+
+// Raises fn's dynamic shared memory limit to the most the current device
+// allows next to its static shared memory (once per kernel and device) and
+// checks that `bytes` fits; cudaErrorInvalidValue when it does not.
+cudaError_t allow_dynamic_smem(const void *fn, size_t bytes);
+
+// Number of SMs of the current device (looked up once per device).
+cudaError_t device_sm_count(int *count);
+
+// Large batches: the counting kernel, then one grid whose first blocks rank
+// the chunks while the others pack the rows of ranked chunks
+// (layout_dispatch_prefill.cu).  layout_dispatch_prefill() says whether these
+// sizes take that path.  wait_ns bounds every wait for a ranked chunk (0: the
+// default); stall_chunk >= 0 leaves that chunk unpublished (tests of the
+// bounded wait only), otherwise -1.
+bool layout_dispatch_prefill(int T, int H, int K, int E, int fp8);
+cudaError_t launch_layout_dispatch_prefill(const int32_t *topk_ids, const void *tokens, int T,
+                                           int H, int K, int E, int R, int fp8,
+                                           int32_t *expert_counts, int32_t *expert_offsets,
+                                           int32_t *rank_offsets, int32_t *src_token,
+                                           int32_t *dst_row, uint32_t *dev_error, void *packed,
+                                           float *scales, void *workspace,
+                                           unsigned long long wait_ns, int stall_chunk,
+                                           cudaStream_t stream);
 
 // Threads per block for `units` work items per row: the largest multiple of
 // 32 up to 256 that divides `units`, else 128 (last block of a row partial).

@@ -32,8 +32,6 @@
 #include "layout_common.cuh"
 #include "moe_layout.h"
 
-#include <mutex>
-
 namespace moe {
 namespace {
 
@@ -50,7 +48,7 @@ constexpr int kScanThreads = 1024;
 __global__ void __launch_bounds__(kThreads)
 layout_count_kernel(const int32_t *__restrict__ ids, int T, int K, int E, int tpc,
                     int chunks, int32_t *__restrict__ ws_cnt,
-                    uint32_t *__restrict__ ws_err)
+                    uint32_t *__restrict__ ws_err, uint32_t *__restrict__ dev_error)
 {
     extern __shared__ __align__(16) int32_t sm[];
     int32_t *hist = sm;                      // [E]
@@ -66,6 +64,8 @@ layout_count_kernel(const int32_t *__restrict__ ids, int T, int K, int E, int tp
     __syncthreads();
     pdl_wait();
     pdl_trigger();
+    // the error word starts at zero; the kernels after this one OR into it
+    if (c == 0 && tid == 0 && dev_error) *dev_error = 0;
     stage_i32(ids_s, ids + (size_t)t0 * K, m);
     cp_async_wait_all();
     __syncthreads();
@@ -251,41 +251,6 @@ size_t rank_smem_bytes(const LayoutPlan &p, int T, int K, int E)
     return sizeof(int32_t) * ((size_t)align4(kWarps * E + E + 1 + extra) + ids);
 }
 
-// Raises a kernel's dynamic shared memory limit to the most the device
-// allows next to the kernel's static shared memory, once per device, and
-// checks that `bytes` fits.
-cudaError_t allow_smem(const void *fn, size_t bytes)
-{
-    static std::mutex mu;
-    static const void *done_fn[8][64];
-    static size_t done_bytes[64][8];
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    std::lock_guard<std::mutex> lock(mu);
-    if (dev < 64)
-        for (auto &row : done_fn)
-            if (row[dev] == fn) return bytes <= done_bytes[dev][&row - done_fn] ? cudaSuccess
-                                                                                 : cudaErrorInvalidValue;
-    int max_optin = 0;
-    e = cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-    if (e != cudaSuccess) return e;
-    cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, fn);
-    if (e != cudaSuccess) return e;
-    const size_t dyn_max = (size_t)max_optin - fa.sharedSizeBytes;
-    if (dyn_max < bytes) return cudaErrorInvalidValue;
-    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn_max);
-    if (e == cudaSuccess && dev < 64)
-        for (auto &row : done_fn)
-            if (row[dev] == nullptr) {
-                row[dev] = fn;
-                done_bytes[dev][&row - done_fn] = dyn_max;
-                break;
-            }
-    return e;
-}
-
 }  // namespace
 
 LayoutPlan plan_layout(int T, int K, int E)
@@ -328,6 +293,18 @@ size_t layout_workspace_bytes(const LayoutPlan &plan, int E)
     return (b + 255) & ~(size_t)255;
 }
 
+cudaError_t launch_layout_count(const int32_t *topk_ids, int T, int K, int E,
+                                const LayoutPlan &p, int32_t *ws_cnt, uint32_t *ws_err,
+                                uint32_t *dev_error, cudaStream_t stream)
+{
+    const size_t csmem = sizeof(int32_t) * ((size_t)align4(E) + (size_t)p.tokens_per_chunk * K);
+    cudaError_t e = allow_dynamic_smem((const void *)layout_count_kernel, csmem);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(layout_count_kernel, dim3(p.chunks), dim3(kThreads), csmem, stream,
+                      topk_ids, T, K, E, p.tokens_per_chunk, p.chunks, ws_cnt, ws_err,
+                      dev_error);
+}
+
 cudaError_t launch_layout(const int32_t *topk_ids, int T, int K, int E, int R,
                           int32_t *expert_counts, int32_t *expert_offsets,
                           int32_t *rank_offsets, int32_t *src_token,
@@ -337,7 +314,7 @@ cudaError_t launch_layout(const int32_t *topk_ids, int T, int K, int E, int R,
     const LayoutPlan p = plan_layout(T, K, E);
     const size_t rsmem = rank_smem_bytes(p, T, K, E);
     if (p.single_launch) {
-        cudaError_t e = allow_smem((const void *)layout_rank_kernel<true>, rsmem);
+        cudaError_t e = allow_dynamic_smem((const void *)layout_rank_kernel<true>, rsmem);
         if (e != cudaSuccess) return e;
         return launch_pdl(layout_rank_kernel<true>, dim3(p.chunks), dim3(kThreads), rsmem,
                           stream, topk_ids, T, K, E, R, p.tokens_per_chunk, p.chunks,
@@ -346,20 +323,16 @@ cudaError_t launch_layout(const int32_t *topk_ids, int T, int K, int E, int R,
     }
     int32_t *ws_cnt = static_cast<int32_t *>(workspace);
     uint32_t *ws_err = reinterpret_cast<uint32_t *>(ws_cnt + (size_t)p.chunks * E);
-    const size_t csmem = sizeof(int32_t) * ((size_t)align4(E) + (size_t)p.tokens_per_chunk * K);
-    cudaError_t e = allow_smem((const void *)layout_count_kernel, csmem);
-    if (e != cudaSuccess) return e;
-    e = launch_pdl(layout_count_kernel, dim3(p.chunks), dim3(kThreads), csmem, stream,
-                   topk_ids, T, K, E, p.tokens_per_chunk, p.chunks, ws_cnt, ws_err);
+    cudaError_t e = launch_layout_count(topk_ids, T, K, E, p, ws_cnt, ws_err, dev_error, stream);
     if (e != cudaSuccess) return e;
     const size_t ssmem = sizeof(int32_t) * (size_t)E * p.chunks;
-    e = allow_smem((const void *)layout_scan_kernel, ssmem);
+    e = allow_dynamic_smem((const void *)layout_scan_kernel, ssmem);
     if (e != cudaSuccess) return e;
     e = launch_pdl(layout_scan_kernel, dim3(1), dim3(kScanThreads), ssmem, stream, E, R,
                    p.chunks, ws_cnt, (const uint32_t *)ws_err, expert_counts,
                    expert_offsets, rank_offsets, dev_error);
     if (e != cudaSuccess) return e;
-    e = allow_smem((const void *)layout_rank_kernel<false>, rsmem);
+    e = allow_dynamic_smem((const void *)layout_rank_kernel<false>, rsmem);
     if (e != cudaSuccess) return e;
     return launch_pdl(layout_rank_kernel<false>, dim3(p.chunks), dim3(kThreads), rsmem,
                       stream, topk_ids, T, K, E, R, p.tokens_per_chunk, p.chunks,

@@ -108,11 +108,13 @@ __device__ __forceinline__ void warp_count(const int32_t *ids, int lo, int hi,
 // Gives every valid entry of ids[lo, hi) its slot: the warp's running
 // counter of its id plus the number of lower lanes holding the same id;
 // the highest such lane then advances the counter.  Writes dst_row[first +
-// i] and src_token[slot]; an invalid id gets dst_row -1.
+// i] and src_token[slot]; an invalid id gets dst_row -1.  With slots_out,
+// slot i also goes to slots_out[i].
 template <bool kBallot>
 __device__ __forceinline__ void warp_rank(const int32_t *ids, int lo, int hi, int E,
                                           int K, int first, int lane, int32_t *row,
-                                          int32_t *dst_row, int32_t *src_token)
+                                          int32_t *dst_row, int32_t *src_token,
+                                          int32_t *slots_out = nullptr)
 {
     const int bits = id_bits(E);
     for (int b = lo; b < hi; b += 32) {
@@ -125,8 +127,10 @@ __device__ __forceinline__ void warp_rank(const int32_t *ids, int lo, int hi, in
             const int slot = row[id] + __popc(m & ((1u << lane) - 1u));
             dst_row[first + i] = slot;
             src_token[slot] = (first + i) / K;
+            if (slots_out) slots_out[i] = slot;
         } else if (valid) {
             dst_row[first + i] = -1;
+            if (slots_out) slots_out[i] = -1;
         }
         __syncwarp();
         if (ok && lane == 31 - __clz(m)) row[id] += __popc(m);

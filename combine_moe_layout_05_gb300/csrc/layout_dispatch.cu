@@ -385,6 +385,11 @@ cudaError_t launch_layout_dispatch(const int32_t *topk_ids, const void *tokens,
         MOE_FUSED_RUN(false, kCountInt);
 #undef MOE_FUSED_RUN
     }
+    if (layout_dispatch_prefill(T, H, K, E, fp8))
+        return launch_layout_dispatch_prefill(topk_ids, tokens, T, H, K, E, R, fp8,
+                                              expert_counts, expert_offsets, rank_offsets,
+                                              src_token, dst_row, dev_error, packed, scales,
+                                              workspace, 0, -1, stream);
     cudaError_t e = launch_layout(topk_ids, T, K, E, R, expert_counts, expert_offsets,
                                   rank_offsets, src_token, dst_row, dev_error,
                                   workspace, stream);

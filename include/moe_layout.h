@@ -63,6 +63,8 @@ typedef enum moe_status {
 #define MOE_DEV_ERR_DUPLICATE    2u  /* some token lists one expert twice       */
 #define MOE_DEV_ERR_REGION_OVERFLOW 4u /* moe_dispatch_send: a rank's rows exceed
                                           its private + bulk capacity          */
+#define MOE_DEV_ERR_TIMEOUT 8u       /* moe_layout_dispatch: a bounded wait for a
+                                        row copy expired; outputs unspecified   */
 
 /* Limits of this implementation. */
 #define MOE_MAX_EXPERTS 1024

@@ -97,11 +97,17 @@ def test_combine_host_checks(lib):
 
 
 def test_layout_dispatch_plan_query(lib):
-    # decode shapes run as one kernel, prefill shapes as layout + dispatch
+    # decode shapes run as one kernel; prefill shapes as the counting kernel
+    # plus one rank-and-pack grid; shapes whose ranking blocks would need too
+    # much shared memory for the packing blocks' occupancy (E = 1024) as
+    # count, scan, rank, dispatch
     assert moe.moe_layout_dispatch_kernels(128, 7168, 8, 256, False) == 1
     assert moe.moe_layout_dispatch_kernels(256, 7168, 8, 256, True) == 1
-    assert moe.moe_layout_dispatch_kernels(4096, 7168, 8, 384, False) == 4
-    assert moe.moe_layout_dispatch_kernels(1000, 4096, 8, 128, False) == 4
+    assert moe.moe_layout_dispatch_kernels(4096, 7168, 8, 384, False) == 2
+    assert moe.moe_layout_dispatch_kernels(16384, 4096, 8, 128, True) == 2
+    assert moe.moe_layout_dispatch_kernels(1000, 4096, 8, 128, False) == 2
+    assert moe.moe_layout_dispatch_kernels(5000, 65536, 8, 16, False) == 2
+    assert moe.moe_layout_dispatch_kernels(2000, 1024, 8, 1024, False) == 4
     assert moe.moe_layout_dispatch_kernels(512, 7168, 8, 256, False) == 2
     assert moe.moe_layout_dispatch_kernels(0, 128, 4, 16, False) == 1
     assert moe.moe_layout_dispatch_kernels(128, 100, 8, 256, False) == 0    # H % 8
@@ -185,6 +191,6 @@ def test_error_bits_agree_between_header_and_binding():
     bits = {m.group(1): int(m.group(2))
             for m in re.finditer(r"#define (MOE_DEV_ERR_\w+)\s+(\d+)u", text)}
     assert bits == {"MOE_DEV_ERR_EXPERT_RANGE": 1, "MOE_DEV_ERR_DUPLICATE": 2,
-                    "MOE_DEV_ERR_REGION_OVERFLOW": 4}
+                    "MOE_DEV_ERR_REGION_OVERFLOW": 4, "MOE_DEV_ERR_TIMEOUT": 8}
     for name, v in bits.items():
         assert getattr(moe, name) == v, name
