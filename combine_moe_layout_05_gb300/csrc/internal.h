@@ -83,6 +83,25 @@ cudaError_t allow_dynamic_smem(const void *fn, size_t bytes);
 // Number of SMs of the current device (looked up once per device).
 cudaError_t device_sm_count(int *count);
 
+// Decode batches in one launch of clusters, the n blocks of a token's row
+// sharing the count through distributed shared memory
+// (layout_dispatch_cluster.cu; measured slower than the single-kernel form,
+// so reachable only through a test hook).
+bool layout_dispatch_clustered(int T, int H, int K, int E, int fp8);
+cudaError_t launch_layout_dispatch_cluster(const int32_t *topk_ids, const void *tokens, int T,
+                                           int H, int K, int E, int R, int fp8,
+                                           int32_t *expert_counts, int32_t *expert_offsets,
+                                           int32_t *rank_offsets, int32_t *src_token,
+                                           int32_t *dst_row, uint32_t *dev_error, void *packed,
+                                           float *scales, cudaStream_t stream);
+// The single-kernel form in which every block counts all ids itself.
+cudaError_t launch_layout_dispatch_fused(const int32_t *topk_ids, const void *tokens, int T,
+                                         int H, int K, int E, int R, int fp8,
+                                         int32_t *expert_counts, int32_t *expert_offsets,
+                                         int32_t *rank_offsets, int32_t *src_token,
+                                         int32_t *dst_row, uint32_t *dev_error, void *packed,
+                                         float *scales, cudaStream_t stream);
+
 // Large batches: the counting kernel, then one grid whose first blocks rank
 // the chunks while the others pack the rows of ranked chunks
 // (layout_dispatch_prefill.cu).  layout_dispatch_prefill() says whether these

@@ -362,6 +362,29 @@ bool layout_dispatch_fused(int T, int H, int K, int fp8)
     return plan_fused(T, H, K, fp8 != 0).use;
 }
 
+cudaError_t launch_layout_dispatch_fused(const int32_t *topk_ids, const void *tokens, int T,
+                                         int H, int K, int E, int R, int fp8,
+                                         int32_t *expert_counts, int32_t *expert_offsets,
+                                         int32_t *rank_offsets, int32_t *src_token,
+                                         int32_t *dst_row, uint32_t *dev_error, void *packed,
+                                         float *scales, cudaStream_t stream)
+{
+    const FusedPlan p = plan_fused(T, H, K, fp8 != 0);
+    if (!p.use) return cudaErrorInvalidValue;
+#define MOE_FUSED_RUN(F, M)                                                                 \
+    return run_fused_k<F, M>(p, topk_ids, tokens, T, H, K, E, R, expert_counts, expert_offsets, \
+                             rank_offsets, src_token, dst_row, dev_error, packed, scales,       \
+                             stream)
+    const bool half = (long long)T * K >= kHalfCountMin;
+    if (fp8) {
+        if (half) MOE_FUSED_RUN(true, kCountHalf);
+        MOE_FUSED_RUN(true, kCountInt);
+    }
+    if (half) MOE_FUSED_RUN(false, kCountHalf);
+    MOE_FUSED_RUN(false, kCountInt);
+#undef MOE_FUSED_RUN
+}
+
 cudaError_t launch_layout_dispatch(const int32_t *topk_ids, const void *tokens,
                                    int T, int H, int K, int E, int R, int fp8,
                                    int32_t *expert_counts, int32_t *expert_offsets,
@@ -370,21 +393,12 @@ cudaError_t launch_layout_dispatch(const int32_t *topk_ids, const void *tokens,
                                    void *packed, float *scales, void *workspace,
                                    cudaStream_t stream)
 {
-    const FusedPlan p = plan_fused(T, H, K, fp8 != 0);
-    if (p.use) {
-#define MOE_FUSED_RUN(F, M)                                                                 \
-    return run_fused_k<F, M>(p, topk_ids, tokens, T, H, K, E, R, expert_counts, expert_offsets, \
-                             rank_offsets, src_token, dst_row, dev_error, packed, scales,       \
-                             stream)
-        const bool half = (long long)T * K >= kHalfCountMin;
-        if (fp8) {
-            if (half) MOE_FUSED_RUN(true, kCountHalf);
-            MOE_FUSED_RUN(true, kCountInt);
-        }
-        if (half) MOE_FUSED_RUN(false, kCountHalf);
-        MOE_FUSED_RUN(false, kCountInt);
-#undef MOE_FUSED_RUN
-    }
+    // (the cluster form, layout_dispatch_cluster.cu, measured slower at every
+    // decode shape and is reachable only through the test hook below)
+    if (plan_fused(T, H, K, fp8 != 0).use)
+        return launch_layout_dispatch_fused(topk_ids, tokens, T, H, K, E, R, fp8, expert_counts,
+                                            expert_offsets, rank_offsets, src_token, dst_row,
+                                            dev_error, packed, scales, stream);
     if (layout_dispatch_prefill(T, H, K, E, fp8))
         return launch_layout_dispatch_prefill(topk_ids, tokens, T, H, K, E, R, fp8,
                                               expert_counts, expert_offsets, rank_offsets,
@@ -399,3 +413,32 @@ cudaError_t launch_layout_dispatch(const int32_t *topk_ids, const void *tokens,
 }
 
 }  // namespace moe
+
+// Test hook, deliberately absent from the public header: moe_layout_dispatch
+// for a decode batch in a chosen form (0: every block counts all ids, the
+// form the library uses; 1: the cluster form), for comparisons of the two.
+// Arguments are checked by the caller (tests only).
+extern "C" __attribute__((visibility("default"))) int32_t
+moe_testing_layout_dispatch_decode(const int32_t *topk_ids, const void *tokens, int32_t T,
+                                   int32_t H, int32_t K, int32_t E, int32_t R, int32_t fp8,
+                                   int32_t *expert_counts, int32_t *expert_offsets,
+                                   int32_t *rank_offsets, int32_t *src_token, int32_t *dst_row,
+                                   uint32_t *dev_error, void *packed, float *scales,
+                                   int32_t variant, cudaStream_t stream)
+{
+    cudaError_t e;
+    if (variant == 1) {
+        if (!moe::layout_dispatch_clustered(T, H, K, E, fp8)) return MOE_ERR_INVALID_ARG;
+        e = moe::launch_layout_dispatch_cluster(topk_ids, tokens, T, H, K, E, R, fp8,
+                                                expert_counts, expert_offsets, rank_offsets,
+                                                src_token, dst_row, dev_error, packed, scales,
+                                                stream);
+    } else {
+        if (!moe::layout_dispatch_fused(T, H, K, fp8)) return MOE_ERR_INVALID_ARG;
+        e = moe::launch_layout_dispatch_fused(topk_ids, tokens, T, H, K, E, R, fp8,
+                                              expert_counts, expert_offsets, rank_offsets,
+                                              src_token, dst_row, dev_error, packed, scales,
+                                              stream);
+    }
+    return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}

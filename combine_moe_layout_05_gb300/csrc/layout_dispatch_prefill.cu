@@ -160,7 +160,7 @@ __device__ __forceinline__ void rank_chunk(const int32_t *__restrict__ ids, int 
         for (int idx = tid; idx < G * E4; idx += nthr) {
             const int e4 = idx % E4, g = idx / E4;
             int4 tt = make_int4(0, 0, 0, 0), pp = make_int4(0, 0, 0, 0);
-#pragma unroll 8
+#pragma unroll 16
             for (int q = g; q < chunks; q += G) {
                 const int4 v = __ldg(reinterpret_cast<const int4 *>(ws_cnt + (size_t)q * E) + e4);
                 tt.x += v.x;
@@ -289,7 +289,7 @@ rank_dispatch_kernel(const int32_t *__restrict__ ids, const uint4 *__restrict__ 
     if (tid == 0) {
         uint32_t *flag = ws_err + t / tpc;
         const unsigned long long deadline = global_ns() + wait_ns;
-        unsigned sleep = 32;
+        unsigned sleep = 16;
         int ok = 0;
         while (true) {
             const uint32_t v = ld_acquire(flag);
@@ -299,7 +299,7 @@ rank_dispatch_kernel(const int32_t *__restrict__ ids, const uint4 *__restrict__ 
             }
             if ((v & kAbandonedBit) || global_ns() > deadline) break;
             __nanosleep(sleep);
-            sleep = sleep < 1024 ? 2 * sleep : 1024;
+            sleep = sleep < 128 ? 2 * sleep : 128;
         }
         if (ok) {
             for (int k = 0; k < k_count; ++k)
