@@ -21,10 +21,14 @@ bool layout_supported(int T, int K, int E);
 size_t layout_workspace_bytes(const LayoutPlan &plan, int E);
 
 // The counting kernel of the multi-launch layout alone: chunk histograms to
-// ws_cnt[chunks][E], chunk error bits to ws_err[chunks], dev_error zeroed.
+// ws_cnt[chunks][E], chunk error bits to ws_err[chunks], dev_error zeroed,
+// and, when dst_row_fill is not null, every dst_row entry set to
+// kSlotPending.
+constexpr int32_t kSlotPending = INT32_MIN;
 cudaError_t launch_layout_count(const int32_t *topk_ids, int T, int K, int E,
                                 const LayoutPlan &plan, int32_t *ws_cnt, uint32_t *ws_err,
-                                uint32_t *dev_error, cudaStream_t stream);
+                                uint32_t *dev_error, int32_t *dst_row_fill,
+                                cudaStream_t stream);
 
 cudaError_t launch_layout(const int32_t *topk_ids, int T, int K, int E, int R,
                           int32_t *expert_counts, int32_t *expert_offsets,
@@ -106,7 +110,7 @@ cudaError_t launch_layout_dispatch_fused(const int32_t *topk_ids, const void *to
 // the chunks while the others pack the rows of ranked chunks
 // (layout_dispatch_prefill.cu).  layout_dispatch_prefill() says whether these
 // sizes take that path.  wait_ns bounds every wait for a ranked chunk (0: the
-// default); stall_chunk >= 0 leaves that chunk unpublished (tests of the
+// default); stall_chunk >= 0 leaves that chunk unranked (tests of the
 // bounded wait only), otherwise -1.
 bool layout_dispatch_prefill(int T, int H, int K, int E, int fp8);
 cudaError_t launch_layout_dispatch_prefill(const int32_t *topk_ids, const void *tokens, int T,

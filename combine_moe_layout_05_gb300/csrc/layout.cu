@@ -48,7 +48,8 @@ constexpr int kScanThreads = 1024;
 __global__ void __launch_bounds__(kThreads)
 layout_count_kernel(const int32_t *__restrict__ ids, int T, int K, int E, int tpc,
                     int chunks, int32_t *__restrict__ ws_cnt,
-                    uint32_t *__restrict__ ws_err, uint32_t *__restrict__ dev_error)
+                    uint32_t *__restrict__ ws_err, uint32_t *__restrict__ dev_error,
+                    int32_t *__restrict__ dst_row_fill)
 {
     extern __shared__ __align__(16) int32_t sm[];
     int32_t *hist = sm;                      // [E]
@@ -66,6 +67,10 @@ layout_count_kernel(const int32_t *__restrict__ ids, int T, int K, int E, int tp
     pdl_trigger();
     // the error word starts at zero; the kernels after this one OR into it
     if (c == 0 && tid == 0 && dev_error) *dev_error = 0;
+    // dst_row_fill: the chunk's slots start as kSlotPending, which the
+    // kernel that ranks the chunk overwrites
+    if (dst_row_fill)
+        for (int i = tid; i < m; i += kThreads) dst_row_fill[(size_t)t0 * K + i] = kSlotPending;
     stage_i32(ids_s, ids + (size_t)t0 * K, m);
     cp_async_wait_all();
     __syncthreads();
@@ -295,14 +300,15 @@ size_t layout_workspace_bytes(const LayoutPlan &plan, int E)
 
 cudaError_t launch_layout_count(const int32_t *topk_ids, int T, int K, int E,
                                 const LayoutPlan &p, int32_t *ws_cnt, uint32_t *ws_err,
-                                uint32_t *dev_error, cudaStream_t stream)
+                                uint32_t *dev_error, int32_t *dst_row_fill,
+                                cudaStream_t stream)
 {
     const size_t csmem = sizeof(int32_t) * ((size_t)align4(E) + (size_t)p.tokens_per_chunk * K);
     cudaError_t e = allow_dynamic_smem((const void *)layout_count_kernel, csmem);
     if (e != cudaSuccess) return e;
     return launch_pdl(layout_count_kernel, dim3(p.chunks), dim3(kThreads), csmem, stream,
                       topk_ids, T, K, E, p.tokens_per_chunk, p.chunks, ws_cnt, ws_err,
-                      dev_error);
+                      dev_error, dst_row_fill);
 }
 
 cudaError_t launch_layout(const int32_t *topk_ids, int T, int K, int E, int R,
@@ -323,7 +329,8 @@ cudaError_t launch_layout(const int32_t *topk_ids, int T, int K, int E, int R,
     }
     int32_t *ws_cnt = static_cast<int32_t *>(workspace);
     uint32_t *ws_err = reinterpret_cast<uint32_t *>(ws_cnt + (size_t)p.chunks * E);
-    cudaError_t e = launch_layout_count(topk_ids, T, K, E, p, ws_cnt, ws_err, dev_error, stream);
+    cudaError_t e = launch_layout_count(topk_ids, T, K, E, p, ws_cnt, ws_err, dev_error,
+                                        nullptr, stream);
     if (e != cudaSuccess) return e;
     const size_t ssmem = sizeof(int32_t) * (size_t)E * p.chunks;
     e = allow_dynamic_smem((const void *)layout_scan_kernel, ssmem);

@@ -10,26 +10,27 @@
 // in front of it, which this path hides under the copy's own reads:
 //
 //  * layout_count_kernel (layout.cu) writes each chunk's histogram and error
-//    bits to the workspace (which also clears the chunk's "ranked" flag
-//    below) and zeroes the error word;
+//    bits to the workspace, sets every dst_row entry to kSlotPending and
+//    zeroes the error word;
 //  * rank_dispatch_kernel: its first C blocks each rank one chunk of tokens.
 //    Block c sums the chunk histograms column by column (the per-expert
 //    totals, whose exclusive scan is expert_offsets, and the entries of each
 //    expert in chunks before c), ranks its chunk's entries in the same stable
-//    order as moe_layout (per-warp counters, warp match), writes dst_row and
-//    src_token, and publishes the chunk: a release-ordered set of the top
-//    bit of its error word.  Every other block packs one slice of one token
-//    row, like moe_dispatch: it loads its 16-byte pieces (and in the FP8 form
-//    quantises them) first, then waits for its token's chunk to be
-//    published, reads the token's K slots and stores.  So the token rows
-//    stream in while the chunks are ranked, and no separate scan, ranking or
-//    dispatch launch sits between the counts and the copy.
+//    order as moe_layout (per-warp counters, warp match) and writes dst_row
+//    and src_token.  Every other block packs one slice of one token row, like
+//    moe_dispatch: its first threads read the token's K slots while all of
+//    them load their 16-byte pieces (and in the FP8 form quantise them); a
+//    slot still kSlotPending is read again until its chunk's ranking block
+//    has written it; then the pieces are stored.  So the token rows stream in
+//    while the chunks are ranked, a packing block whose chunk is ranked pays
+//    one memory round trip as in moe_dispatch, and no separate scan, ranking
+//    or dispatch launch sits between the counts and the copy.
 //
 // The ranking blocks come first in the grid, so they are scheduled before
 // any packing block that waits for them.  Each wait is bounded: past its
-// deadline the block marks the chunk abandoned (so the chunk's other blocks
-// stop waiting at once), sets MOE_DEV_ERR_TIMEOUT in the error word and
-// returns without storing.
+// deadline the block marks the chunk abandoned in the workspace (so the
+// chunk's other blocks stop waiting at once), sets MOE_DEV_ERR_TIMEOUT in the
+// error word and returns without storing.
 #include "common.cuh"
 #include "internal.h"
 #include "layout_common.cuh"
@@ -39,9 +40,7 @@
 namespace moe {
 namespace {
 
-constexpr uint32_t kRankedBit = 0x80000000u;     // ws_err[c]: chunk c's slots are written
-constexpr uint32_t kAbandonedBit = 0x40000000u;  // ws_err[c]: a wait for chunk c expired
-constexpr uint32_t kFlagBits = kRankedBit | kAbandonedBit;
+constexpr uint32_t kAbandonedBit = 0x80000000u;  // ws_err[c]: a wait for chunk c expired
 constexpr unsigned long long kWaitNs = 1000000000ull;   // 1 s
 constexpr size_t kMaxRankSmem = 24 * 1024;       // keeps packing blocks at full occupancy
 constexpr size_t kSmemPerSm = 228 * 1024;        // shared memory of one SM (sm_100 family)
@@ -54,13 +53,8 @@ __device__ __forceinline__ uint64_t global_ns()
     return t;
 }
 
-__device__ __forceinline__ uint32_t ld_acquire(const uint32_t *p)
-{
-    uint32_t v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
+// Loads that observe other blocks' writes made during this kernel (device
+// scope, no stale first-level cache line).
 __device__ __forceinline__ int32_t ld_relaxed(const int32_t *p)
 {
     int32_t v;
@@ -68,9 +62,11 @@ __device__ __forceinline__ int32_t ld_relaxed(const int32_t *p)
     return v;
 }
 
-__device__ __forceinline__ void or_release(uint32_t *p, uint32_t v)
+__device__ __forceinline__ uint32_t ld_relaxed(const uint32_t *p)
 {
-    asm volatile("red.release.gpu.global.or.b32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
 }
 
 // Exclusive scan of hist[0..E) into off[0..E] (off[E] = total) by the whole
@@ -200,8 +196,7 @@ __device__ __forceinline__ void rank_chunk(const int32_t *__restrict__ ids, int 
     }
     if (c == 0) {
         uint32_t err = 0;
-        for (int q = tid; q < chunks; q += nthr)
-            err |= *reinterpret_cast<volatile const uint32_t *>(ws_err + q) & ~kFlagBits;
+        for (int q = tid; q < chunks; q += nthr) err |= ld_relaxed(ws_err + q) & ~kAbandonedBit;
         if (err) atomicOr(&s_err, err);
     }
     cp_async_wait_all();
@@ -234,10 +229,8 @@ __device__ __forceinline__ void rank_chunk(const int32_t *__restrict__ ids, int 
         }
     }
     __syncthreads();
+    if (c == stall_chunk) return;           // test hook: the chunk's slots stay pending
     warp_rank<false>(ids_s, lo, hi, E, K, first, lane, rows + w * E, dst_row, src_token);
-    __threadfence();
-    __syncthreads();
-    if (tid == 0 && c != stall_chunk) or_release(ws_err + c, kRankedBit);
 }
 
 // KT > 0: K known at compile time.  Blocks [0, chunks) rank; block
@@ -261,7 +254,6 @@ rank_dispatch_kernel(const int32_t *__restrict__ ids, const uint4 *__restrict__ 
         return;
     }
     __shared__ int32_t s_slots[MOE_MAX_TOPK];
-    __shared__ int s_ok;
     const int q = b - chunks;
     const int t = q / slices, sl = q - (q / slices) * slices;
     const int tid = threadIdx.x;
@@ -272,7 +264,8 @@ rank_dispatch_kernel(const int32_t *__restrict__ ids, const uint4 *__restrict__ 
     pdl_wait();
     pdl_trigger();
 
-    // the row piece first: it arrives while the chunk is being ranked
+    // the row piece and the token's K slots are requested together; the
+    // piece arrives while the chunk is being ranked
     uint4 a = make_uint4(0, 0, 0, 0), bv = make_uint4(0, 0, 0, 0);
     if (active) {
         if (kFp8) {
@@ -282,36 +275,33 @@ rank_dispatch_kernel(const int32_t *__restrict__ ids, const uint4 *__restrict__ 
             a = ld_stream_v4(tokens + (size_t)t * vrow + u);
         }
     }
+    const int32_t *my_slot = dst_row + (size_t)t * k_count + tid;
+    int32_t slot = tid < k_count ? ld_relaxed(my_slot) : 0;
     Fp8Piece p;
     if (kFp8) p = quantize16(a, bv);     // every lane takes part (shuffles)
 
-    // wait until the token's chunk is ranked, then take its K slots
-    if (tid == 0) {
-        uint32_t *flag = ws_err + t / tpc;
+    // a slot still pending is read again until its chunk's ranking block has
+    // written it (bounded; an expired wait abandons the chunk)
+    int ok = 1;
+    if (tid < k_count && slot == kSlotPending) {
+        uint32_t *chunk_err = ws_err + t / tpc;
         const unsigned long long deadline = global_ns() + wait_ns;
         unsigned sleep = 16;
-        int ok = 0;
         while (true) {
-            const uint32_t v = ld_acquire(flag);
-            if (v & kRankedBit) {
-                ok = 1;
-                break;
-            }
-            if ((v & kAbandonedBit) || global_ns() > deadline) break;
             __nanosleep(sleep);
             sleep = sleep < 128 ? 2 * sleep : 128;
+            slot = ld_relaxed(my_slot);
+            if (slot != kSlotPending) break;
+            if ((ld_relaxed(chunk_err) & kAbandonedBit) || global_ns() > deadline) {
+                atomicOr(chunk_err, kAbandonedBit);
+                if (dev_error) atomicOr(dev_error, MOE_DEV_ERR_TIMEOUT);
+                ok = 0;
+                break;
+            }
         }
-        if (ok) {
-            for (int k = 0; k < k_count; ++k)
-                s_slots[k] = ld_relaxed(dst_row + (size_t)t * k_count + k);
-        } else {
-            atomicOr(flag, kAbandonedBit);
-            if (dev_error) atomicOr(dev_error, MOE_DEV_ERR_TIMEOUT);
-        }
-        s_ok = ok;
     }
-    __syncthreads();
-    if (!s_ok || !active) return;
+    if (tid < k_count) s_slots[tid] = slot;
+    if (!__syncthreads_and(ok) || !active) return;
     const int rows = T * k_count;
     if (kFp8)
         store_fp8_to_slots<KT>(s_slots, k_count, rows, packed, scales, H, u, p);
@@ -410,7 +400,7 @@ cudaError_t launch_layout_dispatch_prefill(const int32_t *topk_ids, const void *
     int32_t *ws_cnt = static_cast<int32_t *>(workspace);
     uint32_t *ws_err = reinterpret_cast<uint32_t *>(ws_cnt + (size_t)pp.lp.chunks * E);
     cudaError_t e = launch_layout_count(topk_ids, T, K, E, pp.lp, ws_cnt, ws_err, dev_error,
-                                        stream);
+                                        dst_row, stream);
     if (e != cudaSuccess) return e;
     if (wait_ns == 0) wait_ns = kWaitNs;
     if (fp8)
@@ -427,11 +417,11 @@ cudaError_t launch_layout_dispatch_prefill(const int32_t *topk_ids, const void *
 
 // Test hook, deliberately absent from the public header: the large-batch
 // path of moe_layout_dispatch with a chosen bound on every wait for a
-// ranked chunk and, when stall_chunk >= 0, that chunk never published (its
-// ranking block writes the slots but never sets the flag).  A test uses it
-// to see the bounded wait expire: the chunk's packing blocks set
-// MOE_DEV_ERR_TIMEOUT and return, every other row is packed, and the
-// context stays usable.  Arguments are checked by the caller (tests only).
+// ranked chunk and, when stall_chunk >= 0, that chunk never ranked (its
+// ranking block stops before writing the slots, which stay pending).  A test
+// uses it to see the bounded wait expire: the chunk's packing blocks set
+// MOE_DEV_ERR_TIMEOUT and return, every other row is packed, and the context
+// stays usable.  Arguments are checked by the caller (tests only).
 extern "C" __attribute__((visibility("default"))) int32_t
 moe_testing_layout_dispatch_prefill(const int32_t *topk_ids, const void *tokens, int32_t T,
                                     int32_t H, int32_t K, int32_t E, int32_t R, int32_t fp8,

@@ -171,12 +171,16 @@ def _hook(lib):
     return f
 
 
+SLOT_PENDING = -2**31      # a dst_row entry not yet written by its chunk's ranking block
+
+
 @pytest.mark.parametrize("fp8", [0, 1])
 def test_bounded_wait_expires_and_reports(oracle, fp8):
-    """Chunk 1 is ranked but never published, and each wait is bounded at
-    2 ms: the call completes, the error word is exactly the timeout bit, the
-    layout is complete, every row of a token outside chunk 1 is packed, and
-    the next normal call on the same context is bit-exact."""
+    """Chunk 1 is never ranked (its slots stay pending) and each wait is
+    bounded at 2 ms: the call completes, the error word is exactly the
+    timeout bit, the counts, offsets and every other chunk's slots are right,
+    every row of a token outside chunk 1 is packed, chunk 1's rows are left
+    alone, and the next normal call on the same context is bit-exact."""
     T, H, K, E, R = 4000, 1024, 8, 64, 8
     assert moe.moe_layout_dispatch_kernels(T, H, K, E, fp8) == 2
     tpc = 1024 // K                      # tokens per chunk at this size
@@ -195,13 +199,27 @@ def test_bounded_wait_expires_and_reports(oracle, fp8):
     assert st == 0
     torch.cuda.synchronize()
     assert time.time() - t0 < 30
+    assert int(buf.dev_error.item()) == MOE_DEV_ERR_TIMEOUT
+    assert np.array_equal(buf.expert_counts.cpu().numpy(), ref.expert_counts)
+    assert np.array_equal(buf.expert_offsets.cpu().numpy(), ref.expert_offsets)
+    assert np.array_equal(buf.rank_offsets.cpu().numpy(), ref.rank_offsets)
+    dr = buf.dst_row.cpu().numpy()
+    assert np.all(dr[tpc:2 * tpc] == SLOT_PENDING)
+    assert np.array_equal(dr[:tpc], ref.dst_row[:tpc])
+    assert np.array_equal(dr[2 * tpc:], ref.dst_row[2 * tpc:])
     others = np.unique(np.concatenate([ref.dst_row[:tpc].ravel(), ref.dst_row[2 * tpc:].ravel()]))
-    _check(oracle, buf, ref, x, packed, scales, T, K, E, R, fp8, rows=others,
-           err=MOE_DEV_ERR_TIMEOUT)
     stalled = np.unique(ref.dst_row[tpc:2 * tpc].ravel())
+    st_tok = buf.src_token.cpu().numpy()
+    assert np.array_equal(st_tok[others], ref.src_token[others])
     if fp8:
+        ec, es = oracle.dispatch_fp8(x, ref.dst_row)
+        assert np.array_equal(packed.view(torch.uint8).cpu().numpy()[others], ec[others])
+        assert np.array_equal(scales.cpu().numpy().view(np.uint32)[others],
+                              es.view(np.uint32)[others])
         assert np.all(packed.view(torch.uint8).cpu().numpy()[stalled] == 0x7F)
     else:
+        exp = oracle.dispatch_bf16(x, ref.dst_row)
+        assert np.array_equal(bf16_host(packed)[others], exp[others])
         assert np.all(bf16_host(packed)[stalled] == 0xFFFF)
     # the context is still usable
     buf2 = _poisoned_layout(T, K, E, R)
