@@ -85,6 +85,12 @@ def parse_args(argv=None):
     p.add_argument("--private", type=int, default=4, help="private rows per region (--path regions)")
     p.add_argument("--unfused", action="store_true",
                    help="moe_layout + moe_dispatch as two calls instead of moe_layout_dispatch")
+    p.add_argument("--variant", choices=("library", "cluster", "persistent", "persistent_bulk"),
+                   default="library",
+                   help="layout+dispatch form (A/B of alternatives the library keeps behind test "
+                        "hooks): cluster = decode batches counted by thread-block clusters; "
+                        "persistent[_bulk] = large batches through one CTA per SM and a "
+                        "shared-memory ring of bulk copies (bulk: bf16 rows stored by bulk copies)")
     p.add_argument("--combine", choices=("bf16", "fp8", "rank_partial"), default="bf16",
                    help="fp8: combine reads the FP8 dispatch output directly "
                         "(moe_combine_fp8, identity experts; needs --dispatch fp8); "
@@ -450,7 +456,39 @@ def expert_outputs(w, dispatch, inp, buf):
     return y.view(torch.int16).cpu().numpy().view("uint16")
 
 
-def step_ops(moe, dispatch, unfused=False, combine="bf16", path="packed"):
+def variant_layout_dispatch(moe, variant, fp8):
+    """moe_layout_dispatch in an alternative form, through the library's test
+    hooks (not part of its public header); returns fn(buffer_set)."""
+    lib = moe.load()
+    P, i32 = ctypes.c_void_p, ctypes.c_int32
+    if variant == "cluster":
+        f = lib.moe_testing_layout_dispatch_decode
+        f.argtypes = [P, P, i32, i32, i32, i32, i32, i32, P, P, P, P, P, P, P, P, i32, P]
+    else:
+        f = lib.moe_testing_layout_pack
+        f.argtypes = [P, P, i32, i32, i32, i32, i32, i32, P, P, P, P, P, P, P, P, P,
+                      ctypes.c_uint64, i32, i32, P]
+    f.restype = i32
+
+    def run(b):
+        import torch
+        L = b.layout
+        T, H = b.tokens.shape
+        args = [b.ids.data_ptr(), b.tokens.data_ptr(), T, H, L.K, L.E, L.R, int(fp8),
+                L.expert_counts.data_ptr(), L.expert_offsets.data_ptr(), L.rank_offsets.data_ptr(),
+                L.src_token.data_ptr(), L.dst_row.data_ptr(), L.dev_error.data_ptr(),
+                b.packed.data_ptr(), b.scales.data_ptr() if fp8 else None]
+        s = torch.cuda.current_stream().cuda_stream
+        if variant == "cluster":
+            st = f(*args, 1, s)
+        else:
+            st = f(*args, L.workspace.data_ptr(), 0, -1, int(variant == "persistent_bulk"), s)
+        if st != 0:
+            raise RuntimeError(f"{variant} layout+dispatch refused these sizes (status {st})")
+    return run
+
+
+def step_ops(moe, dispatch, unfused=False, combine="bf16", path="packed", variant="library"):
     """The calls of one step, as (name, fn(buffer_set)) in launch order."""
     fp8 = dispatch == "fp8"
     if path == "regions":
@@ -466,6 +504,8 @@ def step_ops(moe, dispatch, unfused=False, combine="bf16", path="packed"):
         ops = [("layout", lambda b: b.layout.run(b.ids)),
                ("dispatch", lambda b: moe.moe_dispatch(b.tokens, b.layout.dst_row,
                                                        b.packed, b.scales, fp8=fp8))]
+    elif variant != "library":
+        ops = [("layout_dispatch", variant_layout_dispatch(moe, variant, fp8))]
     else:
         ops = [("layout_dispatch", lambda b: b.layout.run_dispatch(
             b.ids, b.tokens, b.packed, b.scales, fp8=fp8))]
@@ -480,8 +520,8 @@ def step_ops(moe, dispatch, unfused=False, combine="bf16", path="packed"):
     return ops
 
 
-def run_step(moe, buf, dispatch, unfused=False, combine="bf16", path="packed"):
-    for _, fn in step_ops(moe, dispatch, unfused, combine, path):
+def run_step(moe, buf, dispatch, unfused=False, combine="bf16", path="packed", variant="library"):
+    for _, fn in step_ops(moe, dispatch, unfused, combine, path, variant):
         fn(buf)
 
 
@@ -597,7 +637,7 @@ def measure_ours(args, w, dispatch, combine, rank, world, local, device, first_l
     inp = wl_inputs(w, rank)
     if combine == "fp8" and dispatch != "fp8":
         raise SystemExit("--combine fp8 needs FP8 dispatch (--dispatch fp8)")
-    ops = step_ops(moe, dispatch, args.unfused, combine, args.path)
+    ops = step_ops(moe, dispatch, args.unfused, combine, args.path, args.variant)
     priv_rows = args.private if args.path == "regions" else None
 
     # rotating buffer sets: total >= 3x L2, so every step starts cold in L2
@@ -612,12 +652,12 @@ def measure_ours(args, w, dispatch, combine, rank, world, local, device, first_l
     del first
     sets = [BufferSet(w, dispatch, inp, y_bits, device, priv_rows) for _ in range(n_sets)]
     for b in sets:                       # eager pass: attributes, parity data
-        run_step(moe, b, dispatch, args.unfused, combine, args.path)
+        run_step(moe, b, dispatch, args.unfused, combine, args.path, args.variant)
     torch.cuda.synchronize()
 
     K = args.steps
     G = max(n_sets, (min(args.graph_steps, max(K, 1)) // n_sets) * n_sets)
-    step = lambda b: run_step(moe, b, dispatch, args.unfused, combine, args.path)
+    step = lambda b: run_step(moe, b, dispatch, args.unfused, combine, args.path, args.variant)
     graphs = StepGraphs(torch, lambda m, sh: [step(sets[j % n_sets]) for j in range(m)], K, G)
     for _ in range(max(1, math.ceil(args.warmup / max(K, 1)))):
         graphs.replay()
@@ -675,7 +715,7 @@ def measure_ours(args, w, dispatch, combine, rank, world, local, device, first_l
                          f"{args.cpu_seconds:.0f} s budget"}
 
     value = world * w.T * K / (pass_ms * 1e-3)
-    lps = launches_per_step(w, dispatch, args.unfused, args.path)
+    lps = launches_per_step(w, dispatch, args.unfused, args.path, args.variant)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s",
         "n_gpus": world, "steps": K, "warmup": args.warmup,
@@ -696,7 +736,7 @@ def measure_ours(args, w, dispatch, combine, rank, world, local, device, first_l
                                                "f32 sum over ranks",
                                "bf16": "bf16 in, f32 accumulate"}[combine],
                    "experts": w.experts, "routing": w.routing,
-                   "calls": [n for n, _ in ops], "path": args.path,
+                   "calls": [n for n, _ in ops], "path": args.path, "variant": args.variant,
                    "l2": f"{n_sets} rotating buffer sets, {n_sets * per_set / 1e6:.0f} MB "
                          f"> 3x L2 ({l2 / 1e6:.0f} MB); every step cold in L2",
                    "launch": f"CUDA graphs of {G} steps, programmatic dependent launch",
@@ -707,7 +747,8 @@ def measure_ours(args, w, dispatch, combine, rank, world, local, device, first_l
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "peak_source": peak_src,
-                     "traffic": profiled_traffic(dom, w.name, dispatch)},
+                     "traffic": (profiled_traffic(dom, w.name, dispatch)
+                                 if args.variant == "library" else None)},
         "e2e": e2e, "gpu_launches": lps * K * len(passes), "launches_per_step": lps,
         "clocks": clocks, "cpu_baseline": cpu, "parity": parity,
     }
@@ -755,9 +796,13 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def launches_per_step(w, dispatch, unfused, path="packed") -> int:
+def launches_per_step(w, dispatch, unfused, path="packed", variant="library") -> int:
     """Kernels this library launches per step (mirrors the C ABI's plans)."""
     import combine_moe_layout_05_gb300 as moe
+    if variant == "cluster":
+        return 2
+    if variant.startswith("persistent"):
+        return 3
     layout_kernels = 1 if moe.moe_layout_workspace_bytes(w.T, w.K, w.E) == 0 else 3
     if path == "regions":
         return layout_kernels + 3
@@ -803,7 +848,7 @@ def run_e2e(args, w, dispatch, combine, inp, sets, n_sets, G, device, torch, moe
             comp.wait_event(up_done)
             if j - n_sets in down_done:       # the set's previous output was read
                 comp.wait_event(down_done[j - n_sets])
-            run_step(moe, b, dispatch, args.unfused, combine, args.path)
+            run_step(moe, b, dispatch, args.unfused, combine, args.path, args.variant)
             comp_done[j] = torch.cuda.Event()
             comp_done[j].record(comp)
             with torch.cuda.stream(down):

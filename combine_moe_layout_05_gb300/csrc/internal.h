@@ -122,6 +122,20 @@ cudaError_t launch_layout_dispatch_prefill(const int32_t *topk_ids, const void *
                                            unsigned long long wait_ns, int stall_chunk,
                                            cudaStream_t stream);
 
+// The persistent form (layout_dispatch_persistent.cu): a shared-memory ring
+// of token rows fed by bulk copies, one CTA per SM; measured slower, so
+// reachable only through a test hook.  bulk_store != 0 writes bf16 rows by
+// bulk copies out of the ring.
+bool layout_dispatch_persistent(int T, int H, int K, int E);
+cudaError_t launch_layout_dispatch_persistent(const int32_t *topk_ids, const void *tokens, int T,
+                                              int H, int K, int E, int R, int fp8,
+                                              int32_t *expert_counts, int32_t *expert_offsets,
+                                              int32_t *rank_offsets, int32_t *src_token,
+                                              int32_t *dst_row, uint32_t *dev_error,
+                                              void *packed, float *scales, void *workspace,
+                                              unsigned long long wait_ns, int stall_cta,
+                                              int bulk_store, cudaStream_t stream);
+
 // Threads per block for `units` work items per row: the largest multiple of
 // 32 up to 256 that divides `units`, else 128 (last block of a row partial).
 int pick_row_block(int units);
