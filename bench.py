@@ -85,12 +85,15 @@ def parse_args(argv=None):
     p.add_argument("--private", type=int, default=4, help="private rows per region (--path regions)")
     p.add_argument("--unfused", action="store_true",
                    help="moe_layout + moe_dispatch as two calls instead of moe_layout_dispatch")
-    p.add_argument("--variant", choices=("library", "cluster", "persistent", "persistent_bulk"),
+    p.add_argument("--variant", choices=("library", "cluster", "decode_bulk", "persistent",
+                                          "persistent_bulk"),
                    default="library",
                    help="layout+dispatch form (A/B of alternatives the library keeps behind test "
                         "hooks): cluster = decode batches counted by thread-block clusters; "
-                        "persistent[_bulk] = large batches through one CTA per SM and a "
-                        "shared-memory ring of bulk copies (bulk: bf16 rows stored by bulk copies)")
+                        "decode_bulk = the decode kernel writing rows by bulk copies out of "
+                        "shared memory (K = 8); persistent[_bulk] = large batches through one CTA "
+                        "per SM and a shared-memory ring of bulk copies (bulk: bf16 rows stored "
+                        "by bulk copies)")
     p.add_argument("--combine", choices=("bf16", "fp8", "rank_partial"), default="bf16",
                    help="fp8: combine reads the FP8 dispatch output directly "
                         "(moe_combine_fp8, identity experts; needs --dispatch fp8); "
@@ -461,7 +464,7 @@ def variant_layout_dispatch(moe, variant, fp8):
     hooks (not part of its public header); returns fn(buffer_set)."""
     lib = moe.load()
     P, i32 = ctypes.c_void_p, ctypes.c_int32
-    if variant == "cluster":
+    if variant in ("cluster", "decode_bulk"):
         f = lib.moe_testing_layout_dispatch_decode
         f.argtypes = [P, P, i32, i32, i32, i32, i32, i32, P, P, P, P, P, P, P, P, i32, P]
     else:
@@ -479,8 +482,8 @@ def variant_layout_dispatch(moe, variant, fp8):
                 L.src_token.data_ptr(), L.dst_row.data_ptr(), L.dev_error.data_ptr(),
                 b.packed.data_ptr(), b.scales.data_ptr() if fp8 else None]
         s = torch.cuda.current_stream().cuda_stream
-        if variant == "cluster":
-            st = f(*args, 1, s)
+        if variant in ("cluster", "decode_bulk"):
+            st = f(*args, 1 if variant == "cluster" else 2, s)
         else:
             st = f(*args, L.workspace.data_ptr(), 0, -1, int(variant == "persistent_bulk"), s)
         if st != 0:
@@ -799,7 +802,7 @@ def run_ours(args):
 def launches_per_step(w, dispatch, unfused, path="packed", variant="library") -> int:
     """Kernels this library launches per step (mirrors the C ABI's plans)."""
     import combine_moe_layout_05_gb300 as moe
-    if variant == "cluster":
+    if variant in ("cluster", "decode_bulk"):
         return 2
     if variant.startswith("persistent"):
         return 3

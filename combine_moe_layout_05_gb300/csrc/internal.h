@@ -106,6 +106,15 @@ cudaError_t launch_layout_dispatch_fused(const int32_t *topk_ids, const void *to
                                          int32_t *dst_row, uint32_t *dev_error, void *packed,
                                          float *scales, cudaStream_t stream);
 
+// The single-kernel form writing its rows by bulk copies out of shared
+// memory (K = 8; measured slower, reachable only through a test hook).
+cudaError_t launch_layout_dispatch_fused_bulk(const int32_t *topk_ids, const void *tokens,
+                                              int T, int H, int K, int E, int R, int fp8,
+                                              int32_t *expert_counts, int32_t *expert_offsets,
+                                              int32_t *rank_offsets, int32_t *src_token,
+                                              int32_t *dst_row, uint32_t *dev_error,
+                                              void *packed, float *scales, cudaStream_t stream);
+
 // Large batches: the counting kernel, then one grid whose first blocks rank
 // the chunks while the others pack the rows of ranked chunks
 // (layout_dispatch_prefill.cu).  layout_dispatch_prefill() says whether these
