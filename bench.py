@@ -86,14 +86,15 @@ def parse_args(argv=None):
     p.add_argument("--unfused", action="store_true",
                    help="moe_layout + moe_dispatch as two calls instead of moe_layout_dispatch")
     p.add_argument("--variant", choices=("library", "cluster", "decode_bulk", "persistent",
-                                          "persistent_bulk"),
+                                          "persistent_bulk", "combine_shuffle"),
                    default="library",
                    help="layout+dispatch form (A/B of alternatives the library keeps behind test "
                         "hooks): cluster = decode batches counted by thread-block clusters; "
                         "decode_bulk = the decode kernel writing rows by bulk copies out of "
                         "shared memory (K = 8); persistent[_bulk] = large batches through one CTA "
                         "per SM and a shared-memory ring of bulk copies (bulk: bf16 rows stored "
-                        "by bulk copies)")
+                        "by bulk copies); combine_shuffle = the bf16 combine with each token's "
+                        "slots and weights loaded by 8 lanes and shuffled to the warp (K = 8)")
     p.add_argument("--combine", choices=("bf16", "fp8", "rank_partial"), default="bf16",
                    help="fp8: combine reads the FP8 dispatch output directly "
                         "(moe_combine_fp8, identity experts; needs --dispatch fp8); "
@@ -507,7 +508,7 @@ def step_ops(moe, dispatch, unfused=False, combine="bf16", path="packed", varian
         ops = [("layout", lambda b: b.layout.run(b.ids)),
                ("dispatch", lambda b: moe.moe_dispatch(b.tokens, b.layout.dst_row,
                                                        b.packed, b.scales, fp8=fp8))]
-    elif variant != "library":
+    elif variant not in ("library", "combine_shuffle"):
         ops = [("layout_dispatch", variant_layout_dispatch(moe, variant, fp8))]
     else:
         ops = [("layout_dispatch", lambda b: b.layout.run_dispatch(
@@ -518,9 +519,29 @@ def step_ops(moe, dispatch, unfused=False, combine="bf16", path="packed", varian
     elif combine == "rank_partial":
         ops.append(("combine_rank_partial", lambda b: moe.moe_combine_rank_partial(
             b.y, b.weights, b.ids, b.layout.dst_row, b.layout.E, b.layout.R, b.out)))
+    elif variant == "combine_shuffle":
+        ops.append(("combine", variant_combine_shuffle(moe)))
     else:
         ops.append(("combine", lambda b: moe.moe_combine(b.y, b.weights, b.layout.dst_row, b.out)))
     return ops
+
+
+def variant_combine_shuffle(moe):
+    """moe_combine in the form kept behind the library's test hook (slots and
+    weights loaded by 8 lanes and shuffled to the warp); returns fn(buffer_set)."""
+    f = moe.load().moe_testing_combine_shfl
+    P, i32 = ctypes.c_void_p, ctypes.c_int32
+    f.argtypes = [P, P, P, i32, i32, i32, P, P]
+    f.restype = i32
+
+    def run(b):
+        import torch
+        T, K = b.weights.shape
+        st = f(b.y.data_ptr(), b.weights.data_ptr(), b.layout.dst_row.data_ptr(), T, b.out.shape[1],
+               K, b.out.data_ptr(), torch.cuda.current_stream().cuda_stream)
+        if st != 0:
+            raise RuntimeError(f"combine_shuffle refused these sizes (status {st})")
+    return run
 
 
 def run_step(moe, buf, dispatch, unfused=False, combine="bf16", path="packed", variant="library"):

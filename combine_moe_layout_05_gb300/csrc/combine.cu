@@ -23,7 +23,11 @@ namespace moe {
 namespace {
 
 // KT > 0 is a compile-time K; otherwise up to kBatch gathers are in flight.
-template <int KT>
+// kShfl (KT <= 32 only): lanes 0 .. K-1 of each warp load the token's slots
+// and weights (one coalesced request each) and shuffles hand them to the
+// warp, instead of every thread loading all K of each (a form kept for
+// comparison, reachable only through the test hook below).
+template <int KT, bool kShfl = false>
 __global__ void __launch_bounds__(256)
 combine_kernel(const uint4 *__restrict__ y, const float *__restrict__ weights,
                const int32_t *__restrict__ dst_row, int K, int vpr, int rows,
@@ -33,7 +37,6 @@ combine_kernel(const uint4 *__restrict__ y, const float *__restrict__ weights,
     pdl_trigger();
     const int t = blockIdx.x;
     const int v = blockIdx.y * blockDim.x + threadIdx.x;
-    if (v >= vpr) return;
     const int k_count = KT > 0 ? KT : K;
     const int32_t *d = dst_row + (size_t)t * k_count;
     const float *wt = weights + (size_t)t * k_count;
@@ -41,6 +44,35 @@ combine_kernel(const uint4 *__restrict__ y, const float *__restrict__ weights,
     float acc[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) acc[j] = 0.0f;
+
+    if (kShfl) {
+        static_assert(!kShfl || (KT > 0 && KT <= 32), "the shuffle form takes a compile-time K <= 32");
+        const int lane = threadIdx.x & 31;
+        const int my_r = lane < KT ? __ldg(d + lane) : -1;
+        const float my_w = lane < KT ? __ldg(wt + lane) : 0.0f;
+        uint4 val[KT > 0 ? KT : 1];
+        float wk[KT > 0 ? KT : 1];
+        bool ok[KT > 0 ? KT : 1];
+#pragma unroll
+        for (int i = 0; i < KT; ++i) {
+            const int r = __shfl_sync(kFullMask, my_r, i);
+            wk[i] = __shfl_sync(kFullMask, my_w, i);
+            ok[i] = (unsigned)r < (unsigned)rows && v < vpr;
+            val[i] = ok[i] ? ld_stream_v4(y + (size_t)r * vpr + v) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int i = 0; i < KT; ++i)
+            if (ok[i]) fma8(acc, wk[i], val[i]);
+        if (v >= vpr) return;
+        uint4 o;
+        o.x = pack_bf16x2_rn(acc[0], acc[1]);
+        o.y = pack_bf16x2_rn(acc[2], acc[3]);
+        o.z = pack_bf16x2_rn(acc[4], acc[5]);
+        o.w = pack_bf16x2_rn(acc[6], acc[7]);
+        st_v4(out + (size_t)t * vpr + v, o);
+        return;
+    }
+    if (v >= vpr) return;
 
     constexpr int B = KT > 0 ? KT : kBatch;
     for (int k0 = 0; k0 < k_count; k0 += B) {
@@ -80,6 +112,18 @@ cudaError_t run_combine(const void *y, const float *w, const int32_t *dst_row,
 
 }  // namespace
 
+cudaError_t launch_combine_shfl(const void *expert_out, const float *topk_weights,
+                                const int32_t *dst_row, int T, int H, int K, void *out,
+                                cudaStream_t stream)
+{
+    if (K != 8) return cudaErrorInvalidValue;
+    const int vpr = H / 8;
+    const int threads = pick_row_block(vpr);
+    return launch_pdl(combine_kernel<8, true>, dim3(T, ceil_div(vpr, threads)), dim3(threads), 0,
+                      stream, static_cast<const uint4 *>(expert_out), topk_weights, dst_row, K,
+                      vpr, T * K, static_cast<uint4 *>(out));
+}
+
 cudaError_t launch_combine(const void *expert_out, const float *topk_weights,
                            const int32_t *dst_row, int T, int H, int K,
                            void *out, cudaStream_t stream)
@@ -95,3 +139,18 @@ cudaError_t launch_combine(const void *expert_out, const float *topk_weights,
 }
 
 }  // namespace moe
+
+// Test hook, deliberately absent from the public header: moe_combine in the
+// form whose lanes 0 .. 7 load the token's slots and weights and shuffle them
+// to the warp (K = 8 only), for comparison with the library's form.
+// Arguments are checked by the caller (tests only).
+extern "C" __attribute__((visibility("default"))) int32_t
+moe_testing_combine_shfl(const void *expert_out, const float *topk_weights,
+                         const int32_t *dst_row, int32_t T, int32_t H, int32_t K, void *out,
+                         cudaStream_t stream)
+{
+    if (K != 8 || T <= 0 || H % 8 != 0) return MOE_ERR_INVALID_ARG;
+    const cudaError_t e = moe::launch_combine_shfl(expert_out, topk_weights, dst_row, T, H, K,
+                                                   out, stream);
+    return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}

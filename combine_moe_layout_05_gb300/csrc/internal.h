@@ -48,6 +48,12 @@ cudaError_t launch_combine(const void *expert_out, const float *topk_weights,
                            const int32_t *dst_row, int T, int H, int K,
                            void *out, cudaStream_t stream);
 
+// moe_combine with the slots and weights loaded by lanes 0..7 and shuffled
+// to the warp (K = 8; reachable only through a test hook).
+cudaError_t launch_combine_shfl(const void *expert_out, const float *topk_weights,
+                                const int32_t *dst_row, int T, int H, int K, void *out,
+                                cudaStream_t stream);
+
 cudaError_t launch_combine_fp8(const void *codes, const float *scales,
                                const float *topk_weights, const int32_t *dst_row,
                                int T, int H, int K, void *out, cudaStream_t stream);
