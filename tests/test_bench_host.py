@@ -121,3 +121,18 @@ def test_reference_arm_runs_on_cpu():
     assert line["cpu_baseline"]["host_cpus"] >= 1 and line["cpu_baseline"]["cpu_model"]
     assert line["e2e"]["h2d_bytes_per_step"] == 0
     assert line["metric"] == bench.METRIC
+
+
+def test_variant_options_and_launch_counts():
+    """--variant picks a form the library keeps behind test hooks; each
+    reports its own launches per step (host-side plan queries only)."""
+    for v in ("library", "cluster", "decode_bulk", "persistent", "persistent_bulk",
+              "combine_shuffle"):
+        assert bench.parse_args(["--variant", v]).variant == v
+    q = wl.get("prefill_qwen3")
+    d = wl.get("decode_dsv3")
+    assert bench.launches_per_step(q, "fp8", False) == 3          # count, rank-and-pack, combine
+    assert bench.launches_per_step(q, "fp8", False, variant="persistent") == 3
+    assert bench.launches_per_step(d, "bf16", False) == 2         # one fused kernel, combine
+    assert bench.launches_per_step(d, "bf16", False, variant="cluster") == 2
+    assert bench.launches_per_step(q, "fp8", True) == 3 + 2       # count, scan, rank; dispatch; combine
