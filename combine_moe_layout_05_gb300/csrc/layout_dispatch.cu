@@ -25,10 +25,12 @@
 //    also counts expert b (count and offset, and the rank offset when b
 //    starts a rank), and block 0 writes the error word.
 // Each block reads all T*K ids, so this path is used only while blocks x
-// entries stays small (decode shapes); the C ABI falls back to moe_layout +
-// moe_dispatch otherwise.  (A form for larger batches, in which each packing
-// block counted only its layout chunk's earlier ids after the counting and
-// scan kernels, replacing the ranking kernel, measured 25-50 % slower.)
+// entries stays small (decode shapes); larger batches take the two-launch
+// path of layout_dispatch_prefill.cu (or moe_layout + moe_dispatch where that
+// path's shared memory would cost too much occupancy).  (A form for larger
+// batches, in which each packing block counted only its layout chunk's
+// earlier ids after the counting and scan kernels, replacing the ranking
+// kernel, measured 25-50 % slower.)
 #include "bulk.cuh"
 #include "common.cuh"
 #include "internal.h"

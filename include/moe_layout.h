@@ -279,13 +279,19 @@ MOE_API moe_status_t moe_dispatch_recv(const void *priv, const float *priv_scale
  * ("Dispatch and Combine").  Every output is bit-identical to calling
  * moe_layout and then moe_dispatch with the same arguments.  For small
  * batches (decode shapes: T*K <= 8192 and a bounded amount of redundant
- * histogram work) it runs as a single kernel launch; larger batches run the
- * layout kernels and then the dispatch kernel.
+ * histogram work) it runs as a single kernel launch.  Larger batches run a
+ * counting kernel and then one grid in which ranking blocks compute the
+ * slots of each chunk of tokens while packing blocks copy every row as soon
+ * as its chunk is ranked (two launches); where that grid's shared memory
+ * would cost too much occupancy (E near 1024) they run moe_layout's kernels
+ * and then the dispatch kernel.  moe_layout_dispatch_kernels() tells which.
  *
  * Arguments are those of moe_layout and moe_dispatch together, with the same
  * layouts, alignment and limits.  workspace: as for moe_layout (a buffer of
  * moe_layout_workspace_bytes(T,K,E) bytes always suffices; the single-kernel
- * path uses none).
+ * path uses none).  dev_error gets moe_layout's bits and, on the two-launch
+ * path, MOE_DEV_ERR_TIMEOUT when a packing block's bounded wait (1 s) for
+ * its chunk's slots expired; the outputs are then unspecified.
  */
 MOE_API moe_status_t moe_layout_dispatch(const int32_t *topk_ids, const void *tokens,
                                          int32_t T, int32_t H, int32_t K, int32_t E,
@@ -297,8 +303,9 @@ MOE_API moe_status_t moe_layout_dispatch(const int32_t *topk_ids, const void *to
                                          cudaStream_t stream);
 
 /* Number of kernel launches moe_layout_dispatch makes for these sizes: 1
- * when it runs as a single kernel, otherwise moe_layout's one or three
- * kernels plus moe_dispatch's one.  0 for invalid sizes. */
+ * when it runs as a single kernel, 2 on the two-launch path, otherwise
+ * moe_layout's one or three kernels plus moe_dispatch's one.  0 for invalid
+ * sizes. */
 MOE_API int32_t moe_layout_dispatch_kernels(int32_t T, int32_t H, int32_t K,
                                             int32_t E, int32_t fp8);
 
