@@ -827,7 +827,7 @@ def launches_per_step(w, dispatch, unfused, path="packed", variant="library") ->
         return 2
     if variant.startswith("persistent"):
         return 3
-    layout_kernels = 1 if moe.moe_layout_workspace_bytes(w.T, w.K, w.E) == 0 else 3
+    layout_kernels = moe.moe_layout_kernels(w.T, w.K, w.E)
     if path == "regions":
         return layout_kernels + 3
     if unfused:

@@ -13,7 +13,7 @@ from ._binding import (MOE_DEV_ERR_DUPLICATE, MOE_DEV_ERR_EXPERT_RANGE,
                        moe_combine_rank_partial,
                        moe_dispatch, moe_dispatch_recv, moe_dispatch_send,
                        moe_layout, moe_layout_dispatch,
-                       moe_layout_dispatch_kernels, moe_layout_static,
+                       moe_layout_dispatch_kernels, moe_layout_kernels, moe_layout_static,
                        moe_layout_workspace_bytes,
                        moe_status_string)
 
@@ -23,7 +23,7 @@ __all__ = [
     "LayoutBuffers",
     "MoeError", "declared_functions", "library_path", "load", "moe_combine",
     "moe_combine_fp8", "moe_combine_rank_partial",
-    "moe_dispatch", "moe_dispatch_recv", "moe_dispatch_send", "moe_layout", "moe_layout_dispatch", "moe_layout_dispatch_kernels", "moe_layout_static",
+    "moe_dispatch", "moe_dispatch_recv", "moe_dispatch_send", "moe_layout", "moe_layout_dispatch", "moe_layout_dispatch_kernels", "moe_layout_kernels", "moe_layout_static",
     "moe_layout_workspace_bytes",
     "moe_status_string",
 ]

@@ -64,6 +64,8 @@ def load(path: str | None = None):
             lib.moe_layout_dispatch.restype = ctypes.c_int
             lib.moe_layout_dispatch_kernels.argtypes = [i32, i32, i32, i32, i32]
             lib.moe_layout_dispatch_kernels.restype = i32
+            lib.moe_layout_kernels.argtypes = [i32, i32, i32]
+            lib.moe_layout_kernels.restype = i32
             lib.moe_combine_fp8.argtypes = [P, P, P, P, i32, i32, i32, P, P]
             lib.moe_combine_fp8.restype = ctypes.c_int
             lib.moe_combine_rank_partial.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, P, P]
@@ -125,6 +127,10 @@ def moe_layout_workspace_bytes(T: int, K: int, E: int) -> int:
 
 def moe_layout_dispatch_kernels(T: int, H: int, K: int, E: int, fp8: bool) -> int:
     return int(load().moe_layout_dispatch_kernels(T, H, K, E, int(bool(fp8))))
+
+
+def moe_layout_kernels(T: int, K: int, E: int) -> int:
+    return int(load().moe_layout_kernels(T, K, E))
 
 
 def moe_layout(topk_ids, E: int, R: int, expert_counts, expert_offsets,

@@ -253,8 +253,14 @@ int32_t moe_layout_dispatch_kernels(int32_t T, int32_t H, int32_t K, int32_t E,
     if ((fp8 != 0 && fp8 != 1) || (fp8 && H % 128 != 0)) return 0;
     if (moe::layout_dispatch_fused(T, H, K, fp8)) return 1;
     if (moe::layout_dispatch_prefill(T, H, K, E, fp8)) return 2;
-    const int layout = moe::plan_layout(T, K, E).single_launch ? 1 : 3;
+    const int layout = moe_layout_kernels(T, K, E);
     return T > 0 ? layout + 1 : layout;
+}
+
+int32_t moe_layout_kernels(int32_t T, int32_t K, int32_t E)
+{
+    if (!layout_sizes_ok(T, K, E)) return 0;
+    return moe::plan_layout(T, K, E).single_launch ? 1 : 3;
 }
 
 }  // extern "C"

@@ -78,6 +78,11 @@ MOE_API const char *moe_status_string(moe_status_t status);
  * moe_layout then rejects. */
 MOE_API size_t moe_layout_workspace_bytes(int32_t T, int32_t K, int32_t E);
 
+/* Number of kernel launches moe_layout makes for these sizes: 1 when the
+ * whole layout fits one launch of self-counting blocks, otherwise 3 (count,
+ * scan, rank).  0 for invalid sizes.  A query: nothing is launched. */
+MOE_API int32_t moe_layout_kernels(int32_t T, int32_t K, int32_t E);
+
 /*
  * moe_layout -- routing histogram, exclusive scan and stable slot map.
  *
@@ -304,8 +309,7 @@ MOE_API moe_status_t moe_layout_dispatch(const int32_t *topk_ids, const void *to
 
 /* Number of kernel launches moe_layout_dispatch makes for these sizes: 1
  * when it runs as a single kernel, 2 on the two-launch path, otherwise
- * moe_layout's one or three kernels plus moe_dispatch's one.  0 for invalid
- * sizes. */
+ * moe_layout_kernels() plus moe_dispatch's one.  0 for invalid sizes. */
 MOE_API int32_t moe_layout_dispatch_kernels(int32_t T, int32_t H, int32_t K,
                                             int32_t E, int32_t fp8);
 

@@ -67,6 +67,10 @@ SHAPES = [  # T, K, E, R: single kernel, count/scan/rank, ragged tails, limits
 ]
 
 
+def test_layout_shapes_cover_every_launch_plan():
+    assert {moe.moe_layout_kernels(T, K, E) for T, K, E, _ in SHAPES} == {1, 3}
+
+
 @pytest.mark.parametrize("T,K,E,R", SHAPES)
 def test_layout_shapes(oracle, T, K, E, R):
     rng = np.random.default_rng(T * 131 + K * 7 + E)
