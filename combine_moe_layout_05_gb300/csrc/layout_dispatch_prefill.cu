@@ -233,8 +233,6 @@ __device__ __forceinline__ void rank_chunk(const int32_t *__restrict__ ids, int 
     warp_rank<false>(ids_s, lo, hi, E, K, first, lane, rows + w * E, dst_row, src_token);
 }
 
-// KT > 0: K known at compile time.  Blocks [0, chunks) rank; block
-// chunks + t * slices + s packs slice s of token t.
 // The FP8 form at 40 registers keeps 6 blocks of 256 threads per SM (46
 // registers, 5 blocks, without the bound): 56.5 against 57.0 us at the
 // Kimi-K2 prefill shape, no spills, unchanged at the Qwen3 shape.
@@ -242,6 +240,8 @@ __device__ __forceinline__ void rank_chunk(const int32_t *__restrict__ ids, int 
 #define MOE_RANK_DISPATCH_FP8_MIN_BLOCKS 6
 #endif
 
+// KT > 0: K known at compile time.  Blocks [0, chunks) rank; block
+// chunks + t * slices + s packs slice s of token t.
 template <int KT, bool kFp8>
 __global__ void __launch_bounds__(256, kFp8 ? MOE_RANK_DISPATCH_FP8_MIN_BLOCKS : 1)
 rank_dispatch_kernel(const int32_t *__restrict__ ids, const uint4 *__restrict__ tokens, int T,
