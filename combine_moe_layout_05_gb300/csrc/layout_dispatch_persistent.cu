@@ -289,7 +289,7 @@ rank_pack_kernel(const int32_t *__restrict__ ids, const uint8_t *__restrict__ to
             const uint32_t par = (uint32_t)(j / stages) & 1u;
             uint64_t *bar = (stall_cta == p && j == 0) ? never : full + s;
             // every lane observes the phase itself (that orders the copy engine's
-            // writes before its reads); the warp then acts on one common verdict
+            // writes before its reads); the warp then acts on one common decision
             const bool ok = mbar_wait_or_abort(bar, par, global_ns() + wait_ns, abort);
             if (!__all_sync(kFullMask, ok)) {
                 *abort = 1;
