@@ -8,12 +8,14 @@
 // packed buffer is both the send buffer and the grouped-GEMM input, so the
 // receive-side copy disappears.
 //
-// Both kernels are HBM-bound copies.  A block covers one token and a slice
-// of its row; each thread reads its 16-byte piece once (read-only path, no
-// L1 allocation), keeps it in registers and writes it to all K slots.  A
-// warp's stores to one slot cover 512 contiguous bytes, so every write is
-// fully coalesced.  The FP8 kernel gives 8 consecutive threads one 1x128
-// block (16 values each), see rowops.cuh.
+// Both kernels are HBM-bound copies.  A block of kRowThreads threads covers
+// kRowThreads consecutive 16-byte pieces of the flat sequence of all token
+// rows (so it may span a row boundary); each thread reads its piece once
+// (read-only path, no L1 allocation), keeps it in registers and writes it to
+// all K slots of its token.  A warp's stores to one slot cover up to 512
+// contiguous bytes, so every write is coalesced.  The FP8 kernel gives 8
+// consecutive threads one 1x128 block (16 values each), see rowops.cuh; rows
+// hold a multiple of 8 pieces, so those 8 threads always share a token.
 #include "common.cuh"
 #include "internal.h"
 #include "moe_layout.h"
@@ -24,47 +26,54 @@ namespace {
 
 // KT > 0: K known at compile time (fully unrolled); KT == 0: runtime K.
 template <int KT>
-__global__ void __launch_bounds__(256)
-dispatch_bf16_kernel(const uint4 *__restrict__ tokens, int K, int vpr,
+__global__ void __launch_bounds__(kRowThreads)
+dispatch_bf16_kernel(const uint4 *__restrict__ tokens, int T, int K, int vpr,
                      const int32_t *__restrict__ dst_row, int rows,
                      uint4 *__restrict__ packed)
 {
     pdl_wait();
     pdl_trigger();
-    const int t = blockIdx.x;
-    const int v = blockIdx.y * blockDim.x + threadIdx.x;
-    if (v >= vpr) return;
+    const RowPiece rp = flat_piece(blockIdx.x, vpr, threadIdx.x);
+    if (rp.t >= T) return;
     const int k_count = KT > 0 ? KT : K;
-    const uint4 x = ld_stream_v4(tokens + (size_t)t * vpr + v);
-    store_to_slots<KT>(dst_row + (size_t)t * k_count, k_count, rows,
+    const uint4 x = ld_stream_v4(tokens + (size_t)rp.t * vpr + rp.u);
+    store_to_slots<KT>(dst_row + (size_t)rp.t * k_count, k_count, rows,
                        reinterpret_cast<uint8_t *>(packed), (size_t)vpr * 16,
-                       (size_t)v * 16, x);
+                       (size_t)rp.u * 16, x);
 }
 
+// 40 registers keep 6 blocks (48 warps) per SM; 44 without the bound.
 template <int KT>
-__global__ void __launch_bounds__(256)
-dispatch_fp8_kernel(const uint4 *__restrict__ tokens, int K, int H,
+__global__ void __launch_bounds__(kRowThreads, 6)
+dispatch_fp8_kernel(const uint4 *__restrict__ tokens, int T, int K, int H,
                     const int32_t *__restrict__ dst_row, int rows,
                     uint8_t *__restrict__ packed, float *__restrict__ scales)
 {
     pdl_wait();
     pdl_trigger();
-    const int t = blockIdx.x;
-    const int g = blockIdx.y * blockDim.x + threadIdx.x;   // 16-value group
-    const bool active = g < (H >> 4);
+    const RowPiece rp = flat_piece(blockIdx.x, H >> 4, threadIdx.x);
+    const bool active = rp.t < T;
     const int k_count = KT > 0 ? KT : K;
     uint4 a = make_uint4(0, 0, 0, 0), b = make_uint4(0, 0, 0, 0);
     if (active) {
-        const uint4 *src = tokens + (size_t)t * (H >> 3) + 2 * g;
+        const uint4 *src = tokens + (size_t)rp.t * (H >> 3) + 2 * rp.u;
         a = ld_stream_v4(src);
         b = ld_stream_v4(src + 1);
     }
-    // groups per row is a multiple of 8 and blocks start at multiples of 32
-    // threads, so the 8 lanes of a 128-value block are always together.
+    // every lane takes part in the block's shuffles; the threads past the
+    // last row are whole groups of 8
     const Fp8Piece p = quantize16(a, b);
     if (!active) return;
-    store_fp8_to_slots<KT>(dst_row + (size_t)t * k_count, k_count, rows, packed,
-                           scales, H, g, p);
+    store_fp8_to_slots<KT>(dst_row + (size_t)rp.t * k_count, k_count, rows, packed,
+                           scales, H, rp.u, p);
+}
+
+// Blocks covering T rows of per_row pieces; 0 past the grid limit (2^31 - 1)
+// or the flat indexing's row length.
+unsigned row_blocks(int T, int per_row)
+{
+    const long long n = ((long long)T * per_row + kRowThreads - 1) / kRowThreads;
+    return n <= 0x7fffffffll && per_row < kMaxRowPieces ? (unsigned)n : 0u;
 }
 
 template <int KT>
@@ -72,10 +81,10 @@ cudaError_t run_bf16(const void *tokens, int T, int H, int K,
                      const int32_t *dst_row, void *packed, cudaStream_t s)
 {
     const int vpr = H / 8;
-    const int threads = pick_row_block(vpr);
-    return launch_pdl(dispatch_bf16_kernel<KT>, dim3(T, ceil_div(vpr, threads)),
-                      dim3(threads), 0, s, static_cast<const uint4 *>(tokens), K,
-                      vpr, dst_row, T * K, static_cast<uint4 *>(packed));
+    if (row_blocks(T, vpr) == 0) return cudaErrorInvalidValue;
+    return launch_pdl(dispatch_bf16_kernel<KT>, dim3(row_blocks(T, vpr)), dim3(kRowThreads), 0,
+                      s, static_cast<const uint4 *>(tokens), T, K, vpr, dst_row, T * K,
+                      static_cast<uint4 *>(packed));
 }
 
 template <int KT>
@@ -83,11 +92,10 @@ cudaError_t run_fp8(const void *tokens, int T, int H, int K,
                     const int32_t *dst_row, void *packed, float *scales,
                     cudaStream_t s)
 {
-    const int groups = H / 16;
-    const int threads = pick_row_block(groups);
-    return launch_pdl(dispatch_fp8_kernel<KT>, dim3(T, ceil_div(groups, threads)),
-                      dim3(threads), 0, s, static_cast<const uint4 *>(tokens), K,
-                      H, dst_row, T * K, static_cast<uint8_t *>(packed), scales);
+    if (row_blocks(T, H / 16) == 0) return cudaErrorInvalidValue;
+    return launch_pdl(dispatch_fp8_kernel<KT>, dim3(row_blocks(T, H / 16)), dim3(kRowThreads),
+                      0, s, static_cast<const uint4 *>(tokens), T, K, H, dst_row, T * K,
+                      static_cast<uint8_t *>(packed), scales);
 }
 
 }  // namespace

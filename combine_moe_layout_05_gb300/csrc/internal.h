@@ -20,15 +20,25 @@ LayoutPlan plan_layout(int T, int K, int E);
 bool layout_supported(int T, int K, int E);
 size_t layout_workspace_bytes(const LayoutPlan &plan, int E);
 
+// Where the multi-block layouts keep their state in the workspace, in int32
+// elements from its start: ws_cnt[chunks][E] (chunk histograms), then
+// ws_err[chunks] (chunk error bits), ws_tot[E] (expert totals) and one
+// arrival counter.
+struct WorkspaceLayout {
+    size_t err, tot, sync;   // element offsets
+    size_t bytes;            // bytes used
+};
+WorkspaceLayout workspace_layout(int chunks, int E);
+
 // The counting kernel of the multi-launch layout alone: chunk histograms to
 // ws_cnt[chunks][E], chunk error bits to ws_err[chunks], dev_error zeroed,
-// and, when dst_row_fill is not null, every dst_row entry set to
-// kSlotPending.
+// when dst_row_fill is not null every dst_row entry set to kSlotPending, and
+// and when sync_zero is not null that word zeroed.
 constexpr int32_t kSlotPending = INT32_MIN;
 cudaError_t launch_layout_count(const int32_t *topk_ids, int T, int K, int E,
                                 const LayoutPlan &plan, int32_t *ws_cnt, uint32_t *ws_err,
                                 uint32_t *dev_error, int32_t *dst_row_fill,
-                                cudaStream_t stream);
+                                uint32_t *sync_zero, cudaStream_t stream);
 
 cudaError_t launch_layout(const int32_t *topk_ids, int T, int K, int E, int R,
                           int32_t *expert_counts, int32_t *expert_offsets,

@@ -44,18 +44,22 @@ constexpr int kScanCells = 16 * 1024;    // chunks x E staged by the scan (64 KB
 constexpr int kScanThreads = 1024;
 
 // Multi-launch path, kernel 1: histogram and error bits of chunk c.
-// ws_cnt is chunk-major: ws_cnt[c * E + e].
+// ws_cnt is chunk-major: ws_cnt[c * E + e].  Each warp takes 32 entries at a
+// time and matches equal ids, so one lane adds each distinct id's count (a
+// hot expert costs one shared atomic per warp step, not one per entry); when
+// K divides 32 the tokens' entries are whole lane groups and the same match
+// shows a duplicated id within a token.
 __global__ void __launch_bounds__(kThreads)
 layout_count_kernel(const int32_t *__restrict__ ids, int T, int K, int E, int tpc,
                     int chunks, int32_t *__restrict__ ws_cnt,
                     uint32_t *__restrict__ ws_err, uint32_t *__restrict__ dev_error,
-                    int32_t *__restrict__ dst_row_fill)
+                    int32_t *__restrict__ dst_row_fill, uint32_t *__restrict__ sync_zero)
 {
     extern __shared__ __align__(16) int32_t sm[];
     int32_t *hist = sm;                      // [E]
     int32_t *ids_s = hist + align4(E);       // [tpc * K], 16-byte aligned
     __shared__ uint32_t s_err;
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31;
     const int c = blockIdx.x;
     const int t0 = min(T, c * tpc), t1 = min(T, t0 + tpc);
     const int m = (t1 - t0) * K;
@@ -66,7 +70,10 @@ layout_count_kernel(const int32_t *__restrict__ ids, int T, int K, int E, int tp
     pdl_wait();
     pdl_trigger();
     // the error word starts at zero; the kernels after this one OR into it
-    if (c == 0 && tid == 0 && dev_error) *dev_error = 0;
+    if (c == 0 && tid == 0) {
+        if (dev_error) *dev_error = 0;
+        if (sync_zero) *sync_zero = 0;
+    }
     // dst_row_fill: the chunk's slots start as kSlotPending, which the
     // kernel that ranks the chunk overwrites
     if (dst_row_fill)
@@ -75,11 +82,19 @@ layout_count_kernel(const int32_t *__restrict__ ids, int T, int K, int E, int tp
     cp_async_wait_all();
     __syncthreads();
 
-    for (int i = tid; i < m; i += kThreads) {
-        const int e = ids_s[i];
-        if ((unsigned)e < (unsigned)E) atomicAdd(hist + e, 1);
+    const bool groups = (32 % K) == 0;
+    const unsigned group = K >= 32 ? kFullMask : (((1u << K) - 1u) << (lane - lane % K));
+    uint32_t err = 0;
+    for (int b = tid - lane; b < m; b += kThreads) {
+        const int i = b + lane;
+        const int id = i < m ? ids_s[i] : -1;
+        const bool ok = (unsigned)id < (unsigned)E;
+        const unsigned same = __match_any_sync(kFullMask, ok ? id : -1 - lane);
+        if (ok && lane == __ffs(same) - 1) atomicAdd(hist + id, __popc(same));
+        if (i < m && !ok) err |= MOE_DEV_ERR_EXPERT_RANGE;
+        if (groups && ok && (same & group) != (1u << lane)) err |= MOE_DEV_ERR_DUPLICATE;
     }
-    const uint32_t err = token_errors(ids_s, t1 - t0, K, E);
+    if (!groups) err |= token_errors(ids_s, t1 - t0, K, E);
     if (err) atomicOr(&s_err, err);
     __syncthreads();
     for (int e = tid; e < E; e += kThreads) ws_cnt[(size_t)c * E + e] = hist[e];
@@ -294,21 +309,31 @@ bool layout_supported(int T, int K, int E)
 size_t layout_workspace_bytes(const LayoutPlan &plan, int E)
 {
     if (plan.single_launch) return 0;
-    const size_t b = sizeof(int32_t) * (size_t)plan.chunks * ((size_t)E + 1);
-    return (b + 255) & ~(size_t)255;
+    const WorkspaceLayout w = workspace_layout(plan.chunks, E);
+    return (w.bytes + 255) & ~(size_t)255;
+}
+
+WorkspaceLayout workspace_layout(int chunks, int E)
+{
+    WorkspaceLayout w;
+    w.err = (size_t)chunks * E;
+    w.tot = w.err + (size_t)chunks;
+    w.sync = w.tot + (size_t)E;
+    w.bytes = sizeof(int32_t) * (w.sync + 1);
+    return w;
 }
 
 cudaError_t launch_layout_count(const int32_t *topk_ids, int T, int K, int E,
                                 const LayoutPlan &p, int32_t *ws_cnt, uint32_t *ws_err,
                                 uint32_t *dev_error, int32_t *dst_row_fill,
-                                cudaStream_t stream)
+                                uint32_t *sync_zero, cudaStream_t stream)
 {
     const size_t csmem = sizeof(int32_t) * ((size_t)align4(E) + (size_t)p.tokens_per_chunk * K);
     cudaError_t e = allow_dynamic_smem((const void *)layout_count_kernel, csmem);
     if (e != cudaSuccess) return e;
     return launch_pdl(layout_count_kernel, dim3(p.chunks), dim3(kThreads), csmem, stream,
                       topk_ids, T, K, E, p.tokens_per_chunk, p.chunks, ws_cnt, ws_err,
-                      dev_error, dst_row_fill);
+                      dev_error, dst_row_fill, sync_zero);
 }
 
 cudaError_t launch_layout(const int32_t *topk_ids, int T, int K, int E, int R,
@@ -330,7 +355,7 @@ cudaError_t launch_layout(const int32_t *topk_ids, int T, int K, int E, int R,
     int32_t *ws_cnt = static_cast<int32_t *>(workspace);
     uint32_t *ws_err = reinterpret_cast<uint32_t *>(ws_cnt + (size_t)p.chunks * E);
     cudaError_t e = launch_layout_count(topk_ids, T, K, E, p, ws_cnt, ws_err, dev_error,
-                                        nullptr, stream);
+                                        nullptr, nullptr, stream);
     if (e != cudaSuccess) return e;
     const size_t ssmem = sizeof(int32_t) * (size_t)E * p.chunks;
     e = allow_dynamic_smem((const void *)layout_scan_kernel, ssmem);

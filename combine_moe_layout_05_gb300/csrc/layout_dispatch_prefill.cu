@@ -11,26 +11,30 @@
 //
 //  * layout_count_kernel (layout.cu) writes each chunk's histogram and error
 //    bits to the workspace, sets every dst_row entry to kSlotPending and
-//    zeroes the error word;
-//  * rank_dispatch_kernel: its first C blocks each rank one chunk of tokens.
-//    Block c sums the chunk histograms column by column (the per-expert
-//    totals, whose exclusive scan is expert_offsets, and the entries of each
-//    expert in chunks before c), ranks its chunk's entries in the same stable
-//    order as moe_layout (per-warp counters, warp match) and writes dst_row
-//    and src_token.  Every other block packs one slice of one token row, like
-//    moe_dispatch: its first threads read the token's K slots while all of
-//    them load their 16-byte pieces (and in the FP8 form quantise them); a
-//    slot still kSlotPending is read again until its chunk's ranking block
-//    has written it; then the pieces are stored.  So the token rows stream in
-//    while the chunks are ranked, a packing block whose chunk is ranked pays
-//    one memory round trip as in moe_dispatch, and no separate scan, ranking
-//    or dispatch launch sits between the counts and the copy.
+//    zeroes the error word and the ranking blocks' arrival counter;
+//  * rank_dispatch_kernel: its first C blocks (C <= kMaxRankBlocks) each
+//    rank one chunk of tokens.  Together they turn the histograms into
+//    per-chunk exclusive prefixes and per-expert totals (each block scans a
+//    slice of the expert columns), meet at an arrival counter, and then
+//    block c scans the totals into expert_offsets and writes the dst_row and
+//    src_token entries of its chunk in the same stable order as moe_layout.
+//    Every other block packs 256 consecutive 16-byte pieces of the flat
+//    sequence of all token rows, like moe_dispatch: its first threads read
+//    the K slots of each token it touches while all of them load their
+//    pieces; a slot still kSlotPending is read again until its chunk's
+//    ranking block has written it; then the pieces are (in the FP8 form
+//    quantised and) stored.  So the token rows stream in while the chunks
+//    are ranked, a packing block whose chunk is ranked pays one memory round
+//    trip as in moe_dispatch, and no separate scan, ranking or dispatch
+//    launch sits between the counts and the copy.
 //
 // The ranking blocks come first in the grid, so they are scheduled before
 // any packing block that waits for them.  Each wait is bounded: past its
-// deadline the block marks the chunk abandoned in the workspace (so the
-// chunk's other blocks stop waiting at once), sets MOE_DEV_ERR_TIMEOUT in the
-// error word and returns without storing.
+// deadline a ranking block marks its chunk abandoned in the workspace, and a
+// packing block marks the chunk of the slot it waited for (so the chunk's
+// other blocks stop waiting at once); either sets MOE_DEV_ERR_TIMEOUT in the
+// error word, and the rows of the slots that could not be read stay
+// unwritten.
 #include "common.cuh"
 #include "internal.h"
 #include "layout_common.cuh"
@@ -45,6 +49,7 @@ constexpr unsigned long long kWaitNs = 1000000000ull;   // 1 s
 constexpr size_t kMaxRankSmem = 24 * 1024;       // keeps packing blocks at full occupancy
 constexpr size_t kSmemPerSm = 228 * 1024;        // shared memory of one SM (sm_100 family)
 constexpr int kSmPerBlockLimit = 32;             // resident blocks per SM
+constexpr int kMaxRankBlocks = 128;              // ranking blocks resident together
 
 __device__ __forceinline__ uint64_t global_ns()
 {
@@ -112,86 +117,113 @@ __device__ __forceinline__ void block_scan(const int32_t *hist, int32_t *off, in
     __syncthreads();
 }
 
+// Loads of workspace words that other blocks of this grid write (second-
+// level cache only, so no stale first-level line is seen).
+__device__ __forceinline__ int32_t ld_l2(const int32_t *p) { return __ldcg(p); }
+
+constexpr int kIdBits = 11;               // ids below 2^11 > MOE_MAX_EXPERTS
+constexpr int kRankWarps = kRowThreads / 32;
+constexpr int kColWords = 4;              // histogram words per lane in step 1
+
+// Stable rank of each valid entry of ids[lo, hi) among the equal ids of this
+// warp's segment, 32 entries at a time (a warp match gives the lanes with
+// the same id): ids[i] becomes (rank << kIdBits) | id, or -1 for an id
+// outside [0, E); cnt[e * kRankWarps] ends as the segment's count of e
+// (cnt is this warp's column of the expert-major counter table).
+__device__ __forceinline__ void warp_local_rank(int32_t *ids, int lo, int hi, int E, int lane,
+                                                int32_t *cnt)
+{
+    for (int b = lo; b < hi; b += 32) {
+        const int i = b + lane;
+        const bool valid = i < hi;
+        const int id = valid ? ids[i] : -1;
+        const bool ok = (unsigned)id < (unsigned)E;
+        const unsigned m = match_ids<false>(id, ok, 0, lane);
+        const int r = ok ? cnt[id * kRankWarps] + __popc(m & ((1u << lane) - 1u)) : 0;
+        __syncwarp();
+        if (ok && lane == 31 - __clz(m)) cnt[id * kRankWarps] = r + 1;
+        if (valid) ids[i] = ok ? (r << kIdBits) | id : -1;
+        __syncwarp();
+    }
+}
+
 // Block c (< chunks) of rank_dispatch_kernel: ranks chunk c and publishes it.
+//
+//  1. The block owns expert columns [e0, e0 + ne) of the chunk histograms
+//     (ne = ceil(E / chunks)); its warps turn them into their exclusive
+//     prefix over the chunks, in place, and write the column totals to
+//     ws_tot.  Every histogram word is read
+//     by one block only.  While those words are in flight the block ranks
+//     each entry of its own chunk among the equal ids of its warp's segment.
+//  2. It announces step 1 on the arrival counter (zeroed by the counting
+//     kernel), turns the per-warp counts into per-warp starts, and waits
+//     (bounded) until every ranking block has arrived.  The ranking blocks
+//     are the first blocks of the grid and at most kMaxRankBlocks, so they
+//     are resident together.
+//  3. It reads the totals and its chunk's row of prefixes, scans the totals
+//     into expert_offsets and writes every entry's slot,
+//         offsets[e] + prefix[c][e] + (warp's start for e) + rank in warp,
+//     each entry on its own.
 __device__ __forceinline__ void rank_chunk(const int32_t *__restrict__ ids, int T, int K, int E,
-                                           int R, int tpc, int chunks, int c,
-                                           const int32_t *__restrict__ ws_cnt,
-                                           uint32_t *__restrict__ ws_err,
-                                           int32_t *__restrict__ counts,
-                                           int32_t *__restrict__ offsets,
-                                           int32_t *__restrict__ rank_offsets,
-                                           int32_t *__restrict__ src_token,
-                                           int32_t *__restrict__ dst_row,
-                                           uint32_t *__restrict__ dev_error, int stall_chunk)
+                                        int R, int tpc, int chunks, int c,
+                                        int32_t *__restrict__ ws_cnt,
+                                        uint32_t *__restrict__ ws_err,
+                                        int32_t *__restrict__ ws_tot,
+                                        uint32_t *__restrict__ ws_sync,
+                                        int32_t *__restrict__ counts,
+                                        int32_t *__restrict__ offsets,
+                                        int32_t *__restrict__ rank_offsets,
+                                        int32_t *__restrict__ src_token,
+                                        int32_t *__restrict__ dst_row,
+                                        uint32_t *__restrict__ dev_error,
+                                        unsigned long long wait_ns, int stall_chunk)
 {
     extern __shared__ __align__(16) int32_t sm[];
-    const int nthr = blockDim.x, nw = nthr >> 5;
-    int32_t *tot = sm;                          // [E]
-    int32_t *pre = tot + align4(E);             // [E]
-    int32_t *base = pre + align4(E);            // [E + 1]
-    int32_t *rows = base + align4(E + 1);       // [nw][E]
-    int32_t *ids_s = rows + align4(nw * E);     // [tpc * K], 16-byte aligned
+    constexpr int nthr = kRowThreads;
+    int32_t *tot = sm;                           // [E]
+    int32_t *pre = tot + align4(E);              // [E]
+    int32_t *base = pre + align4(E);             // [E + 1]
+    int32_t *cnt = base + align4(E + 1);         // [E][kRankWarps], 16-byte aligned
+    int32_t *col = cnt + E * kRankWarps;         // [ne][chunks]
+    int32_t *ids_s = col + align4(ceil_div(E, chunks) * chunks);   // [tpc * K], 16-byte aligned
     __shared__ int32_t warp_sums[32];
     __shared__ uint32_t s_err;
+    __shared__ int s_ok;
 
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     const int t0 = min(T, c * tpc), t1 = min(T, t0 + tpc);
     const int first = t0 * K, m = (t1 - t0) * K;
-    for (int e = tid; e < E; e += nthr) {
-        tot[e] = 0;
-        pre[e] = 0;
+    const int ne_max = ceil_div(E, chunks);
+    const int e0 = min(E, c * ne_max), ne = min(E, e0 + ne_max) - e0;
+    // lane holds 2^lp consecutive chunks of a column (chunks <= 32 << lp)
+    const int lp = chunks <= 32 ? 0 : (chunks <= 64 ? 1 : 2);
+    const int q0 = lane << lp;
+    for (int i = tid; i < E * kRankWarps / 4; i += nthr)
+        reinterpret_cast<int4 *>(cnt)[i] = make_int4(0, 0, 0, 0);
+    if (tid == 0) {
+        s_err = 0;
+        s_ok = 1;
     }
-    for (int i = tid; i < nw * E; i += nthr) rows[i] = 0;
-    if (tid == 0) s_err = 0;
     __syncthreads();
     pdl_wait();
     pdl_trigger();
     stage_i32(ids_s, ids + first, m);
 
-    // per-expert totals and entries in earlier chunks: column sums of the
-    // chunk histograms, four experts per 16-byte load where rows allow
-    if ((E & 3) == 0) {
-        const int E4 = E >> 2;
-        const int G = nthr >= E4 ? nthr / E4 : 1;
-        for (int idx = tid; idx < G * E4; idx += nthr) {
-            const int e4 = idx % E4, g = idx / E4;
-            int4 tt = make_int4(0, 0, 0, 0), pp = make_int4(0, 0, 0, 0);
-#pragma unroll 16
-            for (int q = g; q < chunks; q += G) {
-                const int4 v = __ldg(reinterpret_cast<const int4 *>(ws_cnt + (size_t)q * E) + e4);
-                tt.x += v.x;
-                tt.y += v.y;
-                tt.z += v.z;
-                tt.w += v.w;
-                if (q < c) {
-                    pp.x += v.x;
-                    pp.y += v.y;
-                    pp.z += v.z;
-                    pp.w += v.w;
-                }
-            }
-            atomicAdd(tot + 4 * e4, tt.x);
-            atomicAdd(tot + 4 * e4 + 1, tt.y);
-            atomicAdd(tot + 4 * e4 + 2, tt.z);
-            atomicAdd(tot + 4 * e4 + 3, tt.w);
-            atomicAdd(pre + 4 * e4, pp.x);
-            atomicAdd(pre + 4 * e4 + 1, pp.y);
-            atomicAdd(pre + 4 * e4 + 2, pp.z);
-            atomicAdd(pre + 4 * e4 + 3, pp.w);
+    // 1. this warp's histogram words, requested together with the chunk's
+    //    ids (word k: column w + (k >> lp) * kRankWarps, chunk q0 + k % 2^lp);
+    //    then the ranks within each warp's segment; then the columns' prefixes
+    {
+        int32_t hv[kColWords];
+#pragma unroll
+        for (int k = 0; k < kColWords; ++k) {
+            const int j = w + (k >> lp) * kRankWarps, q = q0 + (k & ((1 << lp) - 1));
+            hv[k] = j < ne && q < chunks ? ld_l2(ws_cnt + (size_t)q * E + e0 + j) : 0;
         }
-    } else {
-        const int G = nthr >= E ? nthr / E : 1;
-        for (int idx = tid; idx < G * E; idx += nthr) {
-            const int e = idx % E, g = idx / E;
-            int tt = 0, pp = 0;
-#pragma unroll 8
-            for (int q = g; q < chunks; q += G) {
-                const int v = __ldg(ws_cnt + (size_t)q * E + e);
-                tt += v;
-                pp += q < c ? v : 0;
-            }
-            atomicAdd(tot + e, tt);
-            atomicAdd(pre + e, pp);
+        cp_async_wait_all();
+#pragma unroll
+        for (int k = 0; k < kColWords; ++k) {
+            const int j = w + (k >> lp) * kRankWarps, q = q0 + (k & ((1 << lp) - 1));
+            if (j < ne && q < chunks) col[j * chunks + q] = hv[k];
         }
     }
     if (c == 0) {
@@ -199,7 +231,71 @@ __device__ __forceinline__ void rank_chunk(const int32_t *__restrict__ ids, int 
         for (int q = tid; q < chunks; q += nthr) err |= ld_relaxed(ws_err + q) & ~kAbandonedBit;
         if (err) atomicOr(&s_err, err);
     }
-    cp_async_wait_all();
+    const int seg = ((m + kRankWarps - 1) / kRankWarps + 31) & ~31;
+    const int lo = min(m, w * seg), hi = min(m, lo + seg);
+    __syncthreads();
+    warp_local_rank(ids_s, lo, hi, E, lane, cnt + w);
+    for (int j = w; j < ne; j += kRankWarps) {
+        const int32_t *cj = col + j * chunks;
+        const int q1 = min(chunks, q0 + (1 << lp));
+        int sum = 0;
+        for (int q = q0; q < q1; ++q) sum += cj[q];
+        int x = sum;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int y = __shfl_up_sync(kFullMask, x, d);
+            if (lane >= d) x += y;
+        }
+        int run = x - sum;
+        for (int q = q0; q < q1; ++q) {
+            ws_cnt[(size_t)q * E + e0 + j] = run;
+            run += cj[q];
+        }
+        if (lane == 31) ws_tot[e0 + j] = x;
+    }
+
+    // 2. arrive; per-warp starts while the others arrive; wait for them
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) atomicAdd(ws_sync, 1u);
+    for (int e = tid; e < E; e += nthr) {
+        int32_t *row = cnt + e * kRankWarps;
+        int32_t v[kRankWarps];
+#pragma unroll
+        for (int ww = 0; ww < kRankWarps; ++ww) v[ww] = row[ww];
+        int run = 0;
+#pragma unroll
+        for (int ww = 0; ww < kRankWarps; ++ww) {
+            row[ww] = run;
+            run += v[ww];
+        }
+    }
+    if (tid == 0) {
+        const unsigned long long deadline = global_ns() + wait_ns;
+        while (ld_relaxed(ws_sync) < (uint32_t)chunks) {
+            __nanosleep(32);
+            if (global_ns() > deadline) {
+                s_ok = 0;
+                break;
+            }
+        }
+        __threadfence();
+    }
+    __syncthreads();
+    if (!s_ok) {
+        // the chunk is never ranked: its packing blocks stop waiting
+        if (tid == 0) {
+            atomicOr(ws_err + c, kAbandonedBit);
+            if (dev_error) atomicOr(dev_error, MOE_DEV_ERR_TIMEOUT);
+        }
+        return;
+    }
+
+    // 3. expert offsets, then every entry's slot
+    for (int e = tid; e < E; e += nthr) {
+        tot[e] = ld_l2(ws_tot + e);
+        pre[e] = ld_l2(ws_cnt + (size_t)c * E + e);
+    }
     __syncthreads();
     block_scan(tot, base, E, warp_sums);
     if (c == 0) {
@@ -214,39 +310,42 @@ __device__ __forceinline__ void rank_chunk(const int32_t *__restrict__ ids, int 
         const int epr = E / R;
         for (int r = tid; r <= R; r += nthr) rank_offsets[r] = base[r * epr];
     }
-
-    // stable ranking of the chunk: warp w owns a contiguous segment
-    const int seg = ((m + nw - 1) / nw + 31) & ~31;
-    const int lo = min(m, w * seg), hi = min(m, lo + seg);
-    warp_count<false>(ids_s, lo, hi, E, lane, rows + w * E);
     __syncthreads();
-    for (int e = tid; e < E; e += nthr) {
-        int run = base[e] + pre[e];
-        for (int ww = 0; ww < nw; ++ww) {
-            const int v = rows[ww * E + e];
-            rows[ww * E + e] = run;
-            run += v;
-        }
-    }
+    for (int e = tid; e < E; e += nthr) base[e] += pre[e];
     __syncthreads();
     if (c == stall_chunk) return;           // test hook: the chunk's slots stay pending
-    warp_rank<false>(ids_s, lo, hi, E, K, first, lane, rows + w * E, dst_row, src_token);
+    for (int i = lo + lane; i < hi; i += 32) {
+        const int v = ids_s[i];
+        if (v >= 0) {
+            const int id = v & ((1 << kIdBits) - 1);
+            const int slot = base[id] + cnt[id * kRankWarps + w] + (v >> kIdBits);
+            dst_row[first + i] = slot;
+            src_token[slot] = (first + i) / K;
+        } else {
+            dst_row[first + i] = -1;
+        }
+    }
 }
 
-// The FP8 form at 40 registers keeps 6 blocks of 256 threads per SM (46
-// registers, 5 blocks, without the bound): 56.5 against 57.0 us at the
-// Kimi-K2 prefill shape, no spills, unchanged at the Qwen3 shape.
-#ifndef MOE_RANK_DISPATCH_FP8_MIN_BLOCKS
-#define MOE_RANK_DISPATCH_FP8_MIN_BLOCKS 6
+// At 40 registers both forms keep 6 blocks of 256 threads (48 warps) per SM.
+// The packing blocks stay within them without spilling because the FP8 form
+// quantises after its slots are known (quantising before the wait kept the
+// block's position and slots live across the division calls and spilled);
+// the ranking blocks spill a little, which costs them less than fewer
+// resident packing blocks would.
+#ifndef MOE_RANK_DISPATCH_MIN_BLOCKS
+#define MOE_RANK_DISPATCH_MIN_BLOCKS 6
 #endif
 
 // KT > 0: K known at compile time.  Blocks [0, chunks) rank; block
-// chunks + t * slices + s packs slice s of token t.
+// chunks + q packs pieces [q * kRowThreads, (q + 1) * kRowThreads) of the
+// flat sequence of all rows' pieces.
 template <int KT, bool kFp8>
-__global__ void __launch_bounds__(256, kFp8 ? MOE_RANK_DISPATCH_FP8_MIN_BLOCKS : 1)
+__global__ void __launch_bounds__(kRowThreads, MOE_RANK_DISPATCH_MIN_BLOCKS)
 rank_dispatch_kernel(const int32_t *__restrict__ ids, const uint4 *__restrict__ tokens, int T,
-                     int H, int K, int E, int R, int tpc, int chunks, int slices,
-                     const int32_t *__restrict__ ws_cnt, uint32_t *__restrict__ ws_err,
+                     int H, int K, int E, int R, int tpc, int chunks,
+                     int32_t *__restrict__ ws_cnt, uint32_t *__restrict__ ws_err,
+                     int32_t *__restrict__ ws_tot, uint32_t *__restrict__ ws_sync,
                      int32_t *__restrict__ counts, int32_t *__restrict__ offsets,
                      int32_t *__restrict__ rank_offsets, int32_t *__restrict__ src_token,
                      int32_t *__restrict__ dst_row, uint32_t *__restrict__ dev_error,
@@ -256,44 +355,53 @@ rank_dispatch_kernel(const int32_t *__restrict__ ids, const uint4 *__restrict__ 
     const int k_count = KT > 0 ? KT : K;
     const int b = blockIdx.x;
     if (b < chunks) {
-        rank_chunk(ids, T, k_count, E, R, tpc, chunks, b, ws_cnt, ws_err, counts, offsets,
-                   rank_offsets, src_token, dst_row, dev_error, stall_chunk);
+        rank_chunk(ids, T, k_count, E, R, tpc, chunks, b, ws_cnt, ws_err, ws_tot, ws_sync,
+                   counts, offsets, rank_offsets, src_token, dst_row, dev_error, wait_ns,
+                   stall_chunk);
         return;
     }
-    __shared__ int32_t s_slots[MOE_MAX_TOPK];
-    const int q = b - chunks;
-    const int t = q / slices, sl = q - (q / slices) * slices;
+    // packing block q covers kRowThreads consecutive pieces of the flat
+    // sequence of all rows: tokens t_first .. t_first + n_tok - 1
+    __shared__ int32_t s_slots[kRowThreads];
     const int tid = threadIdx.x;
     const int units = kFp8 ? (H >> 4) : (H >> 3);
-    const int u = sl * blockDim.x + tid;
-    const bool active = u < units;
+    const unsigned q = (unsigned)(b - chunks);
+    const RowPiece start = flat_block_start(q, units);
     const size_t vrow = (size_t)(H >> 3);
     pdl_wait();
     pdl_trigger();
 
-    // the row piece and the token's K slots are requested together; the
+    // the row piece and the block's slots are requested together; the
     // piece arrives while the chunk is being ranked
     uint4 a = make_uint4(0, 0, 0, 0), bv = make_uint4(0, 0, 0, 0);
-    if (active) {
-        if (kFp8) {
-            a = ld_stream_v4(tokens + (size_t)t * vrow + 2 * u);
-            bv = ld_stream_v4(tokens + (size_t)t * vrow + 2 * u + 1);
-        } else {
-            a = ld_stream_v4(tokens + (size_t)t * vrow + u);
+    bool active, has_slot;
+    {
+        const int dt = (start.u + tid) / units, u = start.u + tid - dt * units;
+        active = start.t + dt < T;
+        if (active) {
+            const uint4 *row = tokens + (size_t)(start.t + dt) * vrow;
+            if (kFp8) {
+                a = ld_stream_v4(row + 2 * u);
+                bv = ld_stream_v4(row + 2 * u + 1);
+            } else {
+                a = ld_stream_v4(row + u);
+            }
         }
+        // the K slots of each token the block touches, contiguous in dst_row
+        const int n_slots = min(T - start.t, (start.u + kRowThreads - 1) / units + 1) * k_count;
+        has_slot = tid < n_slots;
+        if (has_slot) s_slots[tid] = ld_relaxed(dst_row + (size_t)start.t * k_count + tid);
     }
-    const int32_t *my_slot = dst_row + (size_t)t * k_count + tid;
-    int32_t slot = tid < k_count ? ld_relaxed(my_slot) : 0;
-    Fp8Piece p;
-    if (kFp8) p = quantize16(a, bv);     // every lane takes part (shuffles)
-
     // a slot still pending is read again until its chunk's ranking block has
-    // written it (bounded; an expired wait abandons the chunk)
-    int ok = 1;
-    if (tid < k_count && slot == kSlotPending) {
-        uint32_t *chunk_err = ws_err + t / tpc;
+    // written it (bounded; an expired wait abandons the chunk and the slot's
+    // row is not written)
+    if (has_slot && s_slots[tid] == kSlotPending) {
+        const int t_first = flat_block_start(q, units).t;
+        const int32_t *my_slot = dst_row + (size_t)t_first * k_count + tid;
+        uint32_t *chunk_err = ws_err + (t_first + tid / k_count) / tpc;
         const unsigned long long deadline = global_ns() + wait_ns;
         unsigned sleep = 16;
+        int32_t slot;
         while (true) {
             __nanosleep(sleep);
             sleep = sleep < 128 ? 2 * sleep : 128;
@@ -302,25 +410,29 @@ rank_dispatch_kernel(const int32_t *__restrict__ ids, const uint4 *__restrict__ 
             if ((ld_relaxed(chunk_err) & kAbandonedBit) || global_ns() > deadline) {
                 atomicOr(chunk_err, kAbandonedBit);
                 if (dev_error) atomicOr(dev_error, MOE_DEV_ERR_TIMEOUT);
-                ok = 0;
+                slot = -1;
                 break;
             }
         }
+        s_slots[tid] = slot;
     }
-    if (tid < k_count) s_slots[tid] = slot;
-    if (!__syncthreads_and(ok) || !active) return;
+    __syncthreads();
+    Fp8Piece p;
+    if (kFp8) p = quantize16(a, bv);     // every lane takes part (shuffles)
+    if (!active) return;
     const int rows = T * k_count;
+    const RowPiece rp = flat_piece(q, units, tid);
+    const int32_t *slots = s_slots + (rp.t - flat_block_start(q, units).t) * k_count;
     if (kFp8)
-        store_fp8_to_slots<KT>(s_slots, k_count, rows, packed, scales, H, u, p);
+        store_fp8_to_slots<KT>(slots, k_count, rows, packed, scales, H, rp.u, p);
     else
-        store_to_slots<KT>(s_slots, k_count, rows, packed, vrow * 16, (size_t)u * 16, a);
+        store_to_slots<KT>(slots, k_count, rows, packed, vrow * 16, (size_t)rp.u * 16, a);
 }
 
 struct PrefillPlan {
     bool use;
-    LayoutPlan lp;
-    int threads;
-    int slices;
+    LayoutPlan lp;          // this path's chunks (at most kMaxRankBlocks)
+    long long pack_blocks;
     size_t smem;
 };
 
@@ -329,24 +441,42 @@ PrefillPlan plan_prefill(int T, int H, int K, int E, bool fp8)
     PrefillPlan pp{};
     pp.lp = plan_layout(T, K, E);
     if (T <= 0 || pp.lp.single_launch) return pp;
+    // the ranking blocks wait for one another, so all of them must be
+    // resident at once: larger chunks where the layout's would be too many
+    // (fewer chunks also need less workspace than the layout's plan)
+    if (pp.lp.chunks > kMaxRankBlocks) {
+        pp.lp.tokens_per_chunk = ceil_div(T, kMaxRankBlocks);
+        pp.lp.chunks = ceil_div(T, pp.lp.tokens_per_chunk);
+    }
+    const int chunks = pp.lp.chunks;
     const int units = fp8 ? H / 16 : H / 8;
-    pp.threads = pick_row_block(units);
-    pp.slices = ceil_div(units, pp.threads);
-    const int nw = pp.threads / 32;
-    pp.smem = sizeof(int32_t) * ((size_t)2 * align4(E) + align4(E + 1) + align4(nw * E) +
-                                 (size_t)pp.lp.tokens_per_chunk * K);
-    const long long grid = (long long)pp.lp.chunks + (long long)T * pp.slices;
+    pp.pack_blocks = ((long long)T * units + kRowThreads - 1) / kRowThreads;
+    const int ne_max = ceil_div(E, chunks);
+    pp.smem = sizeof(int32_t) * ((size_t)2 * align4(E) + align4(E + 1) + (size_t)kRankWarps * E +
+                                 align4(ne_max * chunks) + (size_t)pp.lp.tokens_per_chunk * K);
+    // a packing block's tokens' slots, one per thread at most
+    const long long max_slots = (long long)((units - 1 + kRowThreads - 1) / units + 1) * K;
+    const long long grid = (long long)chunks + pp.pack_blocks;
     // every block carries the ranking blocks' shared memory: take this path
     // only while the packing blocks still fill at least 3/4 of an SM
     const long long per_sm = min((long long)kSmPerBlockLimit, (long long)(kSmemPerSm / (pp.smem + 1024)));
-    pp.use = pp.threads >= 64 && pp.smem <= kMaxRankSmem && per_sm * pp.threads >= 1536 &&
-             grid <= 0x7fffffffll;
+    pp.use = units < kMaxRowPieces && max_slots <= kRowThreads && pp.smem <= kMaxRankSmem &&
+             chunks <= 32 * kColWords &&
+             ne_max <= (kColWords >> (chunks <= 32 ? 0 : (chunks <= 64 ? 1 : 2))) * kRankWarps &&
+             per_sm * kRowThreads >= 1536 && grid <= 0x7fffffffll;
     return pp;
 }
 
+struct PrefillWorkspace {
+    int32_t *cnt;
+    uint32_t *err;
+    int32_t *tot;
+    uint32_t *sync;
+};
+
 template <int KT, bool kFp8>
 cudaError_t run_prefill(const PrefillPlan &pp, const int32_t *ids, const void *tokens, int T,
-                        int H, int K, int E, int R, const int32_t *ws_cnt, uint32_t *ws_err,
+                        int H, int K, int E, int R, const PrefillWorkspace &ws,
                         int32_t *counts, int32_t *offsets, int32_t *rank_offsets,
                         int32_t *src_token, int32_t *dst_row, uint32_t *dev_error,
                         void *packed, float *scales, unsigned long long wait_ns,
@@ -355,26 +485,26 @@ cudaError_t run_prefill(const PrefillPlan &pp, const int32_t *ids, const void *t
     auto *fn = rank_dispatch_kernel<KT, kFp8>;
     cudaError_t e = allow_dynamic_smem((const void *)fn, pp.smem);
     if (e != cudaSuccess) return e;
-    const unsigned grid = (unsigned)(pp.lp.chunks + (long long)T * pp.slices);
-    return launch_pdl(fn, dim3(grid), dim3(pp.threads), pp.smem, s, ids,
+    const unsigned grid = (unsigned)(pp.lp.chunks + pp.pack_blocks);
+    return launch_pdl(fn, dim3(grid), dim3(kRowThreads), pp.smem, s, ids,
                       static_cast<const uint4 *>(tokens), T, H, K, E, R,
-                      pp.lp.tokens_per_chunk, pp.lp.chunks, pp.slices, ws_cnt, ws_err, counts,
-                      offsets, rank_offsets, src_token, dst_row, dev_error,
+                      pp.lp.tokens_per_chunk, pp.lp.chunks, ws.cnt, ws.err, ws.tot, ws.sync,
+                      counts, offsets, rank_offsets, src_token, dst_row, dev_error,
                       static_cast<uint8_t *>(packed), scales, wait_ns, stall_chunk);
 }
 
 template <bool kFp8>
 cudaError_t run_prefill_k(const PrefillPlan &pp, const int32_t *ids, const void *tokens, int T,
-                          int H, int K, int E, int R, const int32_t *ws_cnt, uint32_t *ws_err,
+                          int H, int K, int E, int R, const PrefillWorkspace &ws,
                           int32_t *counts, int32_t *offsets, int32_t *rank_offsets,
                           int32_t *src_token, int32_t *dst_row, uint32_t *dev_error,
                           void *packed, float *scales, unsigned long long wait_ns,
                           int stall_chunk, cudaStream_t s)
 {
 #define MOE_PREFILL_CASE(KV)                                                                   \
-    return run_prefill<KV, kFp8>(pp, ids, tokens, T, H, K, E, R, ws_cnt, ws_err, counts,       \
-                                 offsets, rank_offsets, src_token, dst_row, dev_error, packed, \
-                                 scales, wait_ns, stall_chunk, s)
+    return run_prefill<KV, kFp8>(pp, ids, tokens, T, H, K, E, R, ws, counts, offsets,          \
+                                 rank_offsets, src_token, dst_row, dev_error, packed, scales,  \
+                                 wait_ns, stall_chunk, s)
     switch (K) {
     case 1: MOE_PREFILL_CASE(1);
     case 2: MOE_PREFILL_CASE(2);
@@ -404,20 +534,21 @@ cudaError_t launch_layout_dispatch_prefill(const int32_t *topk_ids, const void *
 {
     const PrefillPlan pp = plan_prefill(T, H, K, E, fp8 != 0);
     if (!pp.use) return cudaErrorInvalidValue;
-    int32_t *ws_cnt = static_cast<int32_t *>(workspace);
-    uint32_t *ws_err = reinterpret_cast<uint32_t *>(ws_cnt + (size_t)pp.lp.chunks * E);
-    cudaError_t e = launch_layout_count(topk_ids, T, K, E, pp.lp, ws_cnt, ws_err, dev_error,
-                                        dst_row, stream);
+    const WorkspaceLayout wl = workspace_layout(pp.lp.chunks, E);
+    int32_t *base = static_cast<int32_t *>(workspace);
+    const PrefillWorkspace ws{base, reinterpret_cast<uint32_t *>(base + wl.err), base + wl.tot,
+                              reinterpret_cast<uint32_t *>(base + wl.sync)};
+    cudaError_t e = launch_layout_count(topk_ids, T, K, E, pp.lp, ws.cnt, ws.err, dev_error,
+                                        dst_row, ws.sync, stream);
     if (e != cudaSuccess) return e;
     if (wait_ns == 0) wait_ns = kWaitNs;
     if (fp8)
-        return run_prefill_k<true>(pp, topk_ids, tokens, T, H, K, E, R, ws_cnt, ws_err,
-                                   expert_counts, expert_offsets, rank_offsets, src_token,
-                                   dst_row, dev_error, packed, scales, wait_ns, stall_chunk,
-                                   stream);
-    return run_prefill_k<false>(pp, topk_ids, tokens, T, H, K, E, R, ws_cnt, ws_err,
-                                expert_counts, expert_offsets, rank_offsets, src_token, dst_row,
-                                dev_error, packed, scales, wait_ns, stall_chunk, stream);
+        return run_prefill_k<true>(pp, topk_ids, tokens, T, H, K, E, R, ws, expert_counts,
+                                   expert_offsets, rank_offsets, src_token, dst_row, dev_error,
+                                   packed, scales, wait_ns, stall_chunk, stream);
+    return run_prefill_k<false>(pp, topk_ids, tokens, T, H, K, E, R, ws, expert_counts,
+                                expert_offsets, rank_offsets, src_token, dst_row, dev_error,
+                                packed, scales, wait_ns, stall_chunk, stream);
 }
 
 }  // namespace moe

@@ -9,6 +9,41 @@
 
 namespace moe {
 
+// Threads per block of the row-copy kernels.  Blocks walk the flat sequence
+// of 16-byte pieces of all token rows, so one block may cover the end of one
+// row and the start of the next: every block size keeps 8 warps whatever H
+// is (a block per row slice would leave 7-warp blocks at H = 7168, and at 40
+// registers only 6 of those fit an SM where 6 of 8 warps do).
+constexpr int kRowThreads = 256;
+constexpr int kMaxRowPieces = 1 << 23;   // pieces per row the flat indexing allows
+
+// Token and piece index within the row.
+struct RowPiece {
+    int t;
+    int u;
+};
+
+// Where block q of kRowThreads pieces starts in rows of per_row pieces:
+// token t = q * kRowThreads / per_row and piece u within it, with 32-bit
+// divisions only (q = A * per_row + B gives q * kRowThreads / per_row =
+// A * kRowThreads + B * kRowThreads / per_row).  Needs per_row < 2^23.
+__device__ __forceinline__ RowPiece flat_block_start(unsigned q, int per_row)
+{
+    const unsigned n = (unsigned)per_row;
+    const unsigned A = q / n, B = q - A * n;
+    const unsigned C = B * kRowThreads, D = C / n;
+    return RowPiece{(int)(A * kRowThreads + D), (int)(C - D * n)};
+}
+
+// Token and piece index of piece `tid` of block q (per_row < 2^23).
+__device__ __forceinline__ RowPiece flat_piece(unsigned q, int per_row, int tid)
+{
+    const RowPiece s = flat_block_start(q, per_row);
+    const int off = s.u + tid;
+    const int dt = off / per_row;
+    return RowPiece{s.t + dt, off - dt * per_row};
+}
+
 // Writes `x` (16 bytes at byte offset `off` of a packed row) to each slot in
 // slots[0 .. k_count); slots outside [0, rows) are skipped.  `slots` may
 // point to global or shared memory or to registers.  KT > 0 is a

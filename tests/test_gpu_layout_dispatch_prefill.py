@@ -90,12 +90,15 @@ PREFILL_SHAPES = [  # T, H, K, E, R, fp8: every one takes the two-launch path
     (4096, 7168, 8, 384, 48, 1),
     (16384, 4096, 8, 128, 16, 1),     # Qwen3 prefill shape
     (16384, 4096, 8, 128, 16, 0),
-    (3001, 1032, 5, 40, 8, 0),        # runtime K, partial packing block per row
+    (3001, 1032, 5, 40, 8, 0),        # runtime K, rows of 129 pieces
     (3001, 1032, 5, 42, 7, 0),        # E % 4 != 0: scalar column sums
     (9001, 512, 1, 16, 4, 0),         # K = 1
     (300, 1024, 32, 64, 4, 1),        # K = 32
     (700, 1024, 9, 64, 4, 1),         # runtime K
-    (5000, 512, 8, 128, 16, 0),       # 64-thread blocks
+    (5000, 512, 8, 128, 16, 0),       # four tokens per packing block
+    (3000, 128, 8, 64, 8, 0),         # 16 or 17 tokens per packing block
+    (6000, 384, 8, 64, 8, 0),         # rows of 48 pieces: warps span two tokens
+    (2500, 2056, 3, 24, 4, 0),        # rows of 257 pieces, K = 3
     (4000, 1024, 8, 64, 8, 1),
     (40000, 1024, 6, 96, 12, 1),
     (100000, 1024, 4, 128, 16, 0),    # chunk count capped by the histogram budget

@@ -156,7 +156,8 @@ def test_dispatch_fp8_special_blocks(oracle):
 
 
 @pytest.mark.parametrize("T,H,K", [(1, 8, 1), (7, 24, 3), (5, 128, 5),
-                                   (130, 1032, 7), (65, 4096, 16), (3, 2048, 32)])
+                                   (130, 1032, 7), (65, 4096, 16), (3, 2048, 32),
+                                   (300, 24, 3), (1000, 1032, 8)])
 def test_dispatch_bf16_shapes(oracle, T, H, K):
     rng = np.random.default_rng(H + K)
     x = wl.to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32))
@@ -167,7 +168,8 @@ def test_dispatch_bf16_shapes(oracle, T, H, K):
 
 
 @pytest.mark.parametrize("T,H,K", [(1, 128, 1), (9, 384, 3), (17, 1152, 6),
-                                   (33, 7168, 9), (2, 128, 32)])
+                                   (33, 7168, 9), (2, 128, 32), (100, 384, 8),
+                                   (513, 640, 4)])
 def test_dispatch_fp8_shapes(oracle, T, H, K):
     rng = np.random.default_rng(H * K + 1)
     x = wl.to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32)
@@ -204,7 +206,8 @@ def test_combine_full_size(oracle, name):
 
 
 @pytest.mark.parametrize("T,H,K", [(1, 8, 1), (7, 24, 3), (5, 128, 5),
-                                   (130, 1032, 7), (65, 4096, 16), (3, 2048, 32)])
+                                   (130, 1032, 7), (65, 4096, 16), (3, 2048, 32),
+                                   (300, 24, 3), (1000, 1032, 8)])
 def test_combine_shapes(oracle, T, H, K):
     rng = np.random.default_rng(T + H + K)
     y = wl.to_bf16_bits((rng.standard_normal((T * K, H)) *
