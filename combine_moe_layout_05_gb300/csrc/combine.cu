@@ -9,15 +9,18 @@
 // acc = +0; acc = fma(w[t,k], y[dst_row[t,k], j], acc) for k = 0..K-1 in
 // order (fp32, round to nearest); out[t, j] = bf16 round-to-nearest-even.
 //
-// HBM-bound gather.  A block covers one token and a slice of its row; each
-// thread owns 8 hidden values (one 16-byte vector), issues all K gathers of
-// its vector before using any of them, then runs the fused multiply-add
-// chain and writes one 16-byte vector.  A warp's K loads each cover 512
-// contiguous bytes of one expert-output row.
+// HBM-bound gather.  A block of kRowThreads threads covers kRowThreads
+// consecutive 16-byte pieces of the flat sequence of all output rows (so it
+// may span a row boundary); each thread owns 8 hidden values (one 16-byte
+// vector), issues all K gathers of its vector before using any of them,
+// then runs the fused multiply-add chain and writes one 16-byte vector.  A
+// warp's K loads each cover up to 512 contiguous bytes of one expert-output
+// row.
 #include "combine_common.cuh"
 #include "common.cuh"
 #include "internal.h"
 #include "moe_layout.h"
+#include "rowops.cuh"
 
 namespace moe {
 namespace {
@@ -27,16 +30,27 @@ namespace {
 // and weights (one coalesced request each) and shuffles hand them to the
 // warp, instead of every thread loading all K of each (a form kept for
 // comparison, reachable only through the test hook below).
-template <int KT, bool kShfl = false>
+// kFlat: blocks walk flat pieces (grid row_blocks(T, vpr)); otherwise one
+// token per block (grid T x row slices), which the shuffle form needs.
+template <int KT, bool kFlat, bool kShfl = false>
 __global__ void __launch_bounds__(256)
 combine_kernel(const uint4 *__restrict__ y, const float *__restrict__ weights,
-               const int32_t *__restrict__ dst_row, int K, int vpr, int rows,
+               const int32_t *__restrict__ dst_row, int T, int K, int vpr, int rows,
                uint4 *__restrict__ out)
 {
+    static_assert(!(kFlat && kShfl), "the shuffle form takes one token per block");
     pdl_wait();
     pdl_trigger();
-    const int t = blockIdx.x;
-    const int v = blockIdx.y * blockDim.x + threadIdx.x;
+    int t, v;
+    if (!kFlat) {
+        t = blockIdx.x;
+        v = blockIdx.y * blockDim.x + threadIdx.x;
+    } else {
+        const RowPiece rp = flat_piece(blockIdx.x, vpr, threadIdx.x);
+        if (rp.t >= T) return;
+        t = rp.t;
+        v = rp.u;
+    }
     const int k_count = KT > 0 ? KT : K;
     const int32_t *d = dst_row + (size_t)t * k_count;
     const float *wt = weights + (size_t)t * k_count;
@@ -104,10 +118,17 @@ cudaError_t run_combine(const void *y, const float *w, const int32_t *dst_row,
                         int T, int H, int K, void *out, cudaStream_t s)
 {
     const int vpr = H / 8;
+    if (flat_rows(T, vpr)) {
+        const unsigned blocks = row_blocks(T, vpr);
+        if (blocks == 0) return cudaErrorInvalidValue;
+        return launch_pdl(combine_kernel<KT, true>, dim3(blocks), dim3(kRowThreads), 0, s,
+                          static_cast<const uint4 *>(y), w, dst_row, T, K, vpr, T * K,
+                          static_cast<uint4 *>(out));
+    }
     const int threads = pick_row_block(vpr);
-    return launch_pdl(combine_kernel<KT>, dim3(T, ceil_div(vpr, threads)),
-                      dim3(threads), 0, s, static_cast<const uint4 *>(y), w,
-                      dst_row, K, vpr, T * K, static_cast<uint4 *>(out));
+    return launch_pdl(combine_kernel<KT, false>, dim3(T, ceil_div(vpr, threads)), dim3(threads),
+                      0, s, static_cast<const uint4 *>(y), w, dst_row, T, K, vpr, T * K,
+                      static_cast<uint4 *>(out));
 }
 
 }  // namespace
@@ -119,9 +140,9 @@ cudaError_t launch_combine_shfl(const void *expert_out, const float *topk_weight
     if (K != 8) return cudaErrorInvalidValue;
     const int vpr = H / 8;
     const int threads = pick_row_block(vpr);
-    return launch_pdl(combine_kernel<8, true>, dim3(T, ceil_div(vpr, threads)), dim3(threads), 0,
-                      stream, static_cast<const uint4 *>(expert_out), topk_weights, dst_row, K,
-                      vpr, T * K, static_cast<uint4 *>(out));
+    return launch_pdl(combine_kernel<8, false, true>, dim3(T, ceil_div(vpr, threads)), dim3(threads), 0,
+                      stream, static_cast<const uint4 *>(expert_out), topk_weights, dst_row, T,
+                      K, vpr, T * K, static_cast<uint4 *>(out));
 }
 
 cudaError_t launch_combine(const void *expert_out, const float *topk_weights,

@@ -68,14 +68,6 @@ dispatch_fp8_kernel(const uint4 *__restrict__ tokens, int T, int K, int H,
                            scales, H, rp.u, p);
 }
 
-// Blocks covering T rows of per_row pieces; 0 past the grid limit (2^31 - 1)
-// or the flat indexing's row length.
-unsigned row_blocks(int T, int per_row)
-{
-    const long long n = ((long long)T * per_row + kRowThreads - 1) / kRowThreads;
-    return n <= 0x7fffffffll && per_row < kMaxRowPieces ? (unsigned)n : 0u;
-}
-
 template <int KT>
 cudaError_t run_bf16(const void *tokens, int T, int H, int K,
                      const int32_t *dst_row, void *packed, cudaStream_t s)

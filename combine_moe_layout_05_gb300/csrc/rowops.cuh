@@ -1,7 +1,7 @@
-// rowops.cuh -- the per-thread pieces of dispatch shared by the plain
-// dispatch kernels and the fused layout+dispatch kernel: writing one 16-byte
-// piece of a token row to all of its slots, and quantising 16 values of a
-// 1x128 block to e4m3 with the block's scale.
+// rowops.cuh -- the per-thread pieces of the row kernels: the flat piece
+// indexing shared by dispatch and combine, writing one 16-byte piece of a
+// token row to all of its slots, and quantising 16 values of a 1x128 block
+// to e4m3 with the block's scale.
 #pragma once
 
 #include "common.cuh"
@@ -33,6 +33,25 @@ __device__ __forceinline__ RowPiece flat_block_start(unsigned q, int per_row)
     const unsigned A = q / n, B = q - A * n;
     const unsigned C = B * kRowThreads, D = C / n;
     return RowPiece{(int)(A * kRowThreads + D), (int)(C - D * n)};
+}
+
+// Blocks of kRowThreads pieces covering T rows of per_row pieces; 0 past
+// the grid limit (2^31 - 1) or the flat indexing's row length.
+inline unsigned row_blocks(int T, int per_row)
+{
+    const long long n = ((long long)T * per_row + kRowThreads - 1) / kRowThreads;
+    return n <= 0x7fffffffll && per_row < kMaxRowPieces ? (unsigned)n : 0u;
+}
+
+// Whether the bf16 combine walks flat pieces: for grids of many waves,
+// where 8-warp blocks keep more warps resident than row slices of fewer
+// threads; single-wave (decode-sized) grids keep one token per block, which
+// measured faster there.  (The dispatch kernels always walk flat pieces; the
+// FP8 combine keeps one token per block, as flat indexing spilled at its 64
+// registers.)
+inline bool flat_rows(int T, int per_row)
+{
+    return (long long)T * per_row >= (1ll << 20) && per_row < kMaxRowPieces;
 }
 
 // Token and piece index of piece `tid` of block q (per_row < 2^23).

@@ -207,7 +207,10 @@ def test_combine_full_size(oracle, name):
 
 @pytest.mark.parametrize("T,H,K", [(1, 8, 1), (7, 24, 3), (5, 128, 5),
                                    (130, 1032, 7), (65, 4096, 16), (3, 2048, 32),
-                                   (300, 24, 3), (1000, 1032, 8)])
+                                   (300, 24, 3), (1000, 1032, 8),
+                                   # grids of >= 2^20 pieces walk flat pieces: blocks
+                                   # spanning 2-3 and 16-17 tokens, ragged last block
+                                   (8200, 1032, 3), (70001, 128, 2)])
 def test_combine_shapes(oracle, T, H, K):
     rng = np.random.default_rng(T + H + K)
     y = wl.to_bf16_bits((rng.standard_normal((T * K, H)) *
