@@ -257,6 +257,7 @@ __device__ __forceinline__ void rank_chunk(const int32_t *__restrict__ ids, int 
     // 2. arrive; per-warp starts while the others arrive; wait for them
     __threadfence();
     __syncthreads();
+    if (c == -2 - stall_chunk) return;      // test hook: this block never arrives
     if (tid == 0) atomicAdd(ws_sync, 1u);
     for (int e = tid; e < E; e += nthr) {
         int32_t *row = cnt + e * kRankWarps;
@@ -554,12 +555,19 @@ cudaError_t launch_layout_dispatch_prefill(const int32_t *topk_ids, const void *
 }  // namespace moe
 
 // Test hook, deliberately absent from the public header: the large-batch
-// path of moe_layout_dispatch with a chosen bound on every wait for a
-// ranked chunk and, when stall_chunk >= 0, that chunk never ranked (its
-// ranking block stops before writing the slots, which stay pending).  A test
-// uses it to see the bounded wait expire: the chunk's packing blocks set
-// MOE_DEV_ERR_TIMEOUT and return, every other row is packed, and the context
-// stays usable.  Arguments are checked by the caller (tests only).
+// path of moe_layout_dispatch with a chosen bound on every wait (for a
+// ranked chunk, and the ranking blocks' wait for one another) and
+//  * stall_chunk >= 0: that chunk never ranked (its ranking block stops
+//    after the arrival barrier, before writing the slots, which stay
+//    pending).  The chunk's packing blocks' waits expire: they set
+//    MOE_DEV_ERR_TIMEOUT and skip its rows; every other row is packed;
+//  * stall_chunk <= -2: ranking block -2 - stall_chunk never arrives at the
+//    barrier, so every other ranking block's wait expires: no chunk is
+//    ranked, every packing block's wait ends (at once for chunks marked
+//    abandoned), and the error word is MOE_DEV_ERR_TIMEOUT;
+//  * stall_chunk == -1: the normal call.
+// Tests use it to see the bounded waits expire with the context still
+// usable.  Arguments are checked by the caller (tests only).
 extern "C" __attribute__((visibility("default"))) int32_t
 moe_testing_layout_dispatch_prefill(const int32_t *topk_ids, const void *tokens, int32_t T,
                                     int32_t H, int32_t K, int32_t E, int32_t R, int32_t fp8,

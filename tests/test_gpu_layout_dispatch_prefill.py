@@ -230,3 +230,41 @@ def test_bounded_wait_expires_and_reports(oracle, fp8):
     buf2.run_dispatch(ids_d, x_d, packed2, scales2, fp8=bool(fp8))
     torch.cuda.synchronize()
     _check(oracle, buf2, ref, x, packed2, scales2, T, K, E, R, fp8)
+
+
+@pytest.mark.parametrize("fp8", [0, 1])
+def test_ranking_barrier_wait_expires_and_reports(oracle, fp8):
+    """Ranking block 2 never arrives at the ranking blocks' barrier and each
+    wait is bounded at 2 ms: every other ranking block gives up and marks its
+    chunk abandoned, every packing block stops waiting, the call completes,
+    the error word is exactly the timeout bit, no slot is written and no row
+    is packed; the next normal call on the same context is bit-exact."""
+    T, H, K, E, R = 4000, 1024, 8, 64, 8
+    assert moe.moe_layout_dispatch_kernels(T, H, K, E, fp8) == 2
+    x, ids = _inputs(T, H, K, E, seed=13)
+    ref = oracle.layout(ids, E, R)
+    buf = _poisoned_layout(T, K, E, R)
+    packed, scales = _outputs(T, H, K, fp8)
+    ids_d, x_d = i32_dev(ids), bf16_dev(x)
+    f = _hook(moe.load())
+    t0 = time.time()
+    st = f(ids_d.data_ptr(), x_d.data_ptr(), T, H, K, E, R, fp8, buf.expert_counts.data_ptr(),
+           buf.expert_offsets.data_ptr(), buf.rank_offsets.data_ptr(), buf.src_token.data_ptr(),
+           buf.dst_row.data_ptr(), buf.dev_error.data_ptr(), packed.data_ptr(),
+           scales.data_ptr() if fp8 else None, buf.workspace.data_ptr(), 2_000_000, -2 - 2,
+           torch.cuda.current_stream().cuda_stream)
+    assert st == 0
+    torch.cuda.synchronize()
+    assert time.time() - t0 < 30
+    assert int(buf.dev_error.item()) == MOE_DEV_ERR_TIMEOUT
+    assert np.all(buf.dst_row.cpu().numpy() == SLOT_PENDING)
+    if fp8:
+        assert np.all(packed.view(torch.uint8).cpu().numpy() == 0x7F)
+    else:
+        assert np.all(bf16_host(packed) == 0xFFFF)
+    # the context is still usable
+    buf2 = _poisoned_layout(T, K, E, R)
+    packed2, scales2 = _outputs(T, H, K, fp8)
+    buf2.run_dispatch(ids_d, x_d, packed2, scales2, fp8=bool(fp8))
+    torch.cuda.synchronize()
+    _check(oracle, buf2, ref, x, packed2, scales2, T, K, E, R, fp8)
