@@ -128,8 +128,8 @@ constexpr int kColWords = 4;              // histogram words per lane in step 1
 // Stable rank of each valid entry of ids[lo, hi) among the equal ids of this
 // warp's segment, 32 entries at a time (a warp match gives the lanes with
 // the same id): ids[i] becomes (rank << kIdBits) | id, or -1 for an id
-// outside [0, E); cnt[e * kRankWarps] ends as the segment's count of e
-// (cnt is this warp's column of the expert-major counter table).
+// outside [0, E); cnt[e] (this warp's row of counters) ends as the
+// segment's count of e.
 __device__ __forceinline__ void warp_local_rank(int32_t *ids, int lo, int hi, int E, int lane,
                                                 int32_t *cnt)
 {
@@ -139,9 +139,9 @@ __device__ __forceinline__ void warp_local_rank(int32_t *ids, int lo, int hi, in
         const int id = valid ? ids[i] : -1;
         const bool ok = (unsigned)id < (unsigned)E;
         const unsigned m = match_ids<false>(id, ok, 0, lane);
-        const int r = ok ? cnt[id * kRankWarps] + __popc(m & ((1u << lane) - 1u)) : 0;
+        const int r = ok ? cnt[id] + __popc(m & ((1u << lane) - 1u)) : 0;
         __syncwarp();
-        if (ok && lane == 31 - __clz(m)) cnt[id * kRankWarps] = r + 1;
+        if (ok && lane == 31 - __clz(m)) cnt[id] = r + 1;
         if (valid) ids[i] = ok ? (r << kIdBits) | id : -1;
         __syncwarp();
     }
@@ -152,9 +152,9 @@ __device__ __forceinline__ void warp_local_rank(int32_t *ids, int lo, int hi, in
 //  1. The block owns expert columns [e0, e0 + ne) of the chunk histograms
 //     (ne = ceil(E / chunks)); its warps turn them into their exclusive
 //     prefix over the chunks, in place, and write the column totals to
-//     ws_tot.  Every histogram word is read
-//     by one block only.  While those words are in flight the block ranks
-//     each entry of its own chunk among the equal ids of its warp's segment.
+//     ws_tot.  Every histogram word is read by one block only.  While those
+//     words are in flight the block ranks each entry of its own chunk among
+//     the equal ids of its warp's segment.
 //  2. It announces step 1 on the arrival counter (zeroed by the counting
 //     kernel), turns the per-warp counts into per-warp starts, and waits
 //     (bounded) until every ranking block has arrived.  The ranking blocks
@@ -183,7 +183,7 @@ __device__ __forceinline__ void rank_chunk(const int32_t *__restrict__ ids, int 
     int32_t *tot = sm;                           // [E]
     int32_t *pre = tot + align4(E);              // [E]
     int32_t *base = pre + align4(E);             // [E + 1]
-    int32_t *cnt = base + align4(E + 1);         // [E][kRankWarps], 16-byte aligned
+    int32_t *cnt = base + align4(E + 1);         // [kRankWarps][E], 16-byte aligned
     int32_t *col = cnt + E * kRankWarps;         // [ne][chunks]
     int32_t *ids_s = col + align4(ceil_div(E, chunks) * chunks);   // [tpc * K], 16-byte aligned
     __shared__ int32_t warp_sums[32];
@@ -234,7 +234,7 @@ __device__ __forceinline__ void rank_chunk(const int32_t *__restrict__ ids, int 
     const int seg = ((m + kRankWarps - 1) / kRankWarps + 31) & ~31;
     const int lo = min(m, w * seg), hi = min(m, lo + seg);
     __syncthreads();
-    warp_local_rank(ids_s, lo, hi, E, lane, cnt + w);
+    warp_local_rank(ids_s, lo, hi, E, lane, cnt + w * E);
     for (int j = w; j < ne; j += kRankWarps) {
         const int32_t *cj = col + j * chunks;
         const int q1 = min(chunks, q0 + (1 << lp));
@@ -260,14 +260,13 @@ __device__ __forceinline__ void rank_chunk(const int32_t *__restrict__ ids, int 
     if (c == -2 - stall_chunk) return;      // test hook: this block never arrives
     if (tid == 0) atomicAdd(ws_sync, 1u);
     for (int e = tid; e < E; e += nthr) {
-        int32_t *row = cnt + e * kRankWarps;
         int32_t v[kRankWarps];
 #pragma unroll
-        for (int ww = 0; ww < kRankWarps; ++ww) v[ww] = row[ww];
+        for (int ww = 0; ww < kRankWarps; ++ww) v[ww] = cnt[ww * E + e];
         int run = 0;
 #pragma unroll
         for (int ww = 0; ww < kRankWarps; ++ww) {
-            row[ww] = run;
+            cnt[ww * E + e] = run;
             run += v[ww];
         }
     }
@@ -319,7 +318,7 @@ __device__ __forceinline__ void rank_chunk(const int32_t *__restrict__ ids, int 
         const int v = ids_s[i];
         if (v >= 0) {
             const int id = v & ((1 << kIdBits) - 1);
-            const int slot = base[id] + cnt[id * kRankWarps + w] + (v >> kIdBits);
+            const int slot = base[id] + cnt[w * E + id] + (v >> kIdBits);
             dst_row[first + i] = slot;
             src_token[slot] = (first + i) / K;
         } else {
