@@ -1,6 +1,6 @@
-// device_info.cu -- per-device facts the launchers need, looked up once per
-// device and kept: the dynamic shared memory limit raised for each kernel
-// and the SM count.
+// device_info.cu -- host-side helpers of the launchers: per-device facts
+// looked up once per device and kept (the dynamic shared memory limit raised
+// for each kernel, the SM count), and the block size of row-slice grids.
 #include "internal.h"
 
 #include <mutex>
@@ -61,6 +61,13 @@ cudaError_t device_sm_count(int *count)
     }
     *count = g_sms[dev];
     return cudaSuccess;
+}
+
+int pick_row_block(int units)
+{
+    for (int b = 256; b >= 64; b -= 32)
+        if (units % b == 0) return b;
+    return units < 128 ? ((units + 31) / 32) * 32 : 128;
 }
 
 }  // namespace moe

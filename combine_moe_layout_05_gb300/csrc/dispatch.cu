@@ -92,13 +92,6 @@ cudaError_t run_fp8(const void *tokens, int T, int H, int K,
 
 }  // namespace
 
-int pick_row_block(int units)
-{
-    for (int b = 256; b >= 64; b -= 32)
-        if (units % b == 0) return b;
-    return units < 128 ? ((units + 31) / 32) * 32 : 128;
-}
-
 cudaError_t launch_dispatch_bf16(const void *tokens, int T, int H, int K,
                                  const int32_t *dst_row, void *packed,
                                  cudaStream_t stream)
