@@ -429,7 +429,8 @@ cudaError_t launch_layout_dispatch_fused_bulk(const int32_t *topk_ids, const voi
                                               void *packed, float *scales, cudaStream_t stream)
 {
     const FusedPlan p = plan_fused(T, H, K, fp8 != 0);
-    if (!p.use || K != 8) return cudaErrorInvalidValue;
+    // the staged form copies one slice per block out of a kThreads-piece stage
+    if (!p.use || K != 8 || p.upc > kThreads) return cudaErrorInvalidValue;
     const bool half = (long long)T * K >= kHalfCountMin;
 #define MOE_BULK_RUN(F, M)                                                                   \
     return run_fused<8, F, M, true>(p, topk_ids, tokens, T, H, K, E, R, expert_counts,        \
