@@ -63,8 +63,9 @@ typedef enum moe_status {
 #define MOE_DEV_ERR_DUPLICATE    2u  /* some token lists one expert twice       */
 #define MOE_DEV_ERR_REGION_OVERFLOW 4u /* moe_dispatch_send: a rank's rows exceed
                                           its private + bulk capacity          */
-#define MOE_DEV_ERR_TIMEOUT 8u       /* moe_layout_dispatch: a bounded wait for a
-                                        row copy expired; outputs unspecified   */
+#define MOE_DEV_ERR_TIMEOUT 8u       /* moe_layout_dispatch: a bounded wait
+                                        between its blocks expired; outputs
+                                        unspecified                            */
 
 /* Limits of this implementation. */
 #define MOE_MAX_EXPERTS 1024
@@ -295,8 +296,9 @@ MOE_API moe_status_t moe_dispatch_recv(const void *priv, const float *priv_scale
  * layouts, alignment and limits.  workspace: as for moe_layout (a buffer of
  * moe_layout_workspace_bytes(T,K,E) bytes always suffices; the single-kernel
  * path uses none).  dev_error gets moe_layout's bits and, on the two-launch
- * path, MOE_DEV_ERR_TIMEOUT when a packing block's bounded wait (1 s) for
- * its chunk's slots expired; the outputs are then unspecified.
+ * path, MOE_DEV_ERR_TIMEOUT when a bounded wait (1 s) expired: a packing
+ * block's wait for its chunk's slots, or a ranking block's wait for the
+ * other ranking blocks; the outputs are then unspecified.
  */
 MOE_API moe_status_t moe_layout_dispatch(const int32_t *topk_ids, const void *tokens,
                                          int32_t T, int32_t H, int32_t K, int32_t E,
