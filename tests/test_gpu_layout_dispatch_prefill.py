@@ -268,3 +268,37 @@ def test_ranking_barrier_wait_expires_and_reports(oracle, fp8):
     buf2.run_dispatch(ids_d, x_d, packed2, scales2, fp8=bool(fp8))
     torch.cuda.synchronize()
     _check(oracle, buf2, ref, x, packed2, scales2, T, K, E, R, fp8)
+
+
+def _random_prefill_shape(rng):
+    """A shape that takes the two-launch path: T*K above the single-kernel
+    sizes, E and H small enough for the ranking blocks' shared memory."""
+    for _ in range(1000):
+        R = int(rng.choice([1, 2, 4, 8, 16]))
+        E = R * int(rng.integers(1, max(2, 320 // R)))
+        K = int(rng.integers(1, min(E, 16) + 1))
+        T = int(rng.integers(8192 // K + 1, 160_000 // K))
+        H = 128 * int(rng.integers(1, 5))
+        fp8 = int(rng.integers(0, 2))
+        if moe.moe_layout_dispatch_kernels(T, H, K, E, fp8) == 2:
+            return T, H, K, E, R, fp8
+    raise AssertionError("no two-launch shape drawn")
+
+
+@pytest.mark.parametrize("case", range(16))
+def test_prefill_path_random_shapes(oracle, case):
+    """Seeded random shapes on the two-launch path (chunk counts up to 128,
+    so each lane of a ranking block holds 1, 2 or 4 words of a histogram
+    column; 1 to 40 expert columns per ranking block), Zipf routing with a
+    few bad ids: every output bit for bit against the oracle."""
+    rng = np.random.default_rng(5000 + case)
+    T, H, K, E, R, fp8 = _random_prefill_shape(rng)
+    x, ids = _inputs(T, H, K, E, seed=6000 + case)
+    if case % 4 == 3:
+        ids[int(rng.integers(0, T)), int(rng.integers(0, K))] = E + 1
+    ref = oracle.layout(ids, E, R)
+    buf = _poisoned_layout(T, K, E, R)
+    packed, scales = _outputs(T, H, K, fp8)
+    buf.run_dispatch(i32_dev(ids), bf16_dev(x), packed, scales, fp8=bool(fp8))
+    torch.cuda.synchronize()
+    _check(oracle, buf, ref, x, packed, scales, T, K, E, R, fp8)
