@@ -260,7 +260,8 @@ int32_t moe_layout_dispatch_kernels(int32_t T, int32_t H, int32_t K, int32_t E,
 int32_t moe_layout_kernels(int32_t T, int32_t K, int32_t E)
 {
     if (!layout_sizes_ok(T, K, E)) return 0;
-    return moe::plan_layout(T, K, E).single_launch ? 1 : 3;
+    if (moe::plan_layout(T, K, E).single_launch) return 1;
+    return moe::layout_ranked(T, K, E) ? 2 : 3;
 }
 
 }  // extern "C"

@@ -33,12 +33,16 @@ WorkspaceLayout workspace_layout(int chunks, int E);
 // The counting kernel of the multi-launch layout alone: chunk histograms to
 // ws_cnt[chunks][E], chunk error bits to ws_err[chunks], dev_error zeroed,
 // when dst_row_fill is not null every dst_row entry set to kSlotPending, and
-// and when sync_zero is not null that word zeroed.
+// and when sync_zero is not null that word zeroed.  threads: 256 or 512 per
+// block (one chunk per block).  512 measured 0.2-0.4 us faster inside the
+// large-batch moe_layout_dispatch at Kimi-K2 sizes (equal at Qwen3), but
+// 5 us slower ahead of moe_layout's ranking-only grid at Qwen3 sizes, where
+// 256 is used.
 constexpr int32_t kSlotPending = INT32_MIN;
 cudaError_t launch_layout_count(const int32_t *topk_ids, int T, int K, int E,
                                 const LayoutPlan &plan, int32_t *ws_cnt, uint32_t *ws_err,
                                 uint32_t *dev_error, int32_t *dst_row_fill,
-                                uint32_t *sync_zero, cudaStream_t stream);
+                                uint32_t *sync_zero, cudaStream_t stream, int threads = 256);
 
 cudaError_t launch_layout(const int32_t *topk_ids, int T, int K, int E, int R,
                           int32_t *expert_counts, int32_t *expert_offsets,
@@ -146,6 +150,16 @@ cudaError_t launch_layout_dispatch_prefill(const int32_t *topk_ids, const void *
                                            float *scales, void *workspace,
                                            unsigned long long wait_ns, int stall_chunk,
                                            cudaStream_t stream);
+
+// moe_layout's large-batch form when its plan fits (layout_dispatch_prefill.cu):
+// the counting kernel, then the ranking blocks of the two-launch
+// layout + dispatch grid alone.  layout_ranked() says whether these sizes take
+// it; otherwise launch_layout runs count, scan and rank.
+bool layout_ranked(int T, int K, int E);
+cudaError_t launch_layout_ranked(const int32_t *topk_ids, int T, int K, int E, int R,
+                                 int32_t *expert_counts, int32_t *expert_offsets,
+                                 int32_t *rank_offsets, int32_t *src_token, int32_t *dst_row,
+                                 uint32_t *dev_error, void *workspace, cudaStream_t stream);
 
 // The persistent form (layout_dispatch_persistent.cu): a shared-memory ring
 // of token rows fed by bulk copies, one CTA per SM; measured slower, so

@@ -37,9 +37,8 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-// Threads of the counting kernel (one 1024-entry chunk per block).  Against
-// 256, 512 took 0.2-0.4 us off the Kimi-K2 prefill layout + dispatch and left
-// Qwen3 unchanged; 1024 helped Kimi-K2 more but cost Qwen3 0.6 us.
+// Most threads of a counting-kernel block; launch_layout_count picks 256 or
+// this many (its `threads`).
 constexpr int kCountThreads = 512;
 constexpr int kSelfMaxEntries = 4096;
 constexpr int kSelfChunk = 256;
@@ -63,12 +62,12 @@ layout_count_kernel(const int32_t *__restrict__ ids, int T, int K, int E, int tp
     int32_t *hist = sm;                      // [E]
     int32_t *ids_s = hist + align4(E);       // [tpc * K], 16-byte aligned
     __shared__ uint32_t s_err;
-    const int tid = threadIdx.x, lane = tid & 31;
+    const int tid = threadIdx.x, lane = tid & 31, nthr = blockDim.x;
     const int c = blockIdx.x;
     const int t0 = min(T, c * tpc), t1 = min(T, t0 + tpc);
     const int m = (t1 - t0) * K;
 
-    for (int e = tid; e < E; e += kCountThreads) hist[e] = 0;
+    for (int e = tid; e < E; e += nthr) hist[e] = 0;
     if (tid == 0) s_err = 0;
     __syncthreads();
     pdl_wait();
@@ -81,7 +80,7 @@ layout_count_kernel(const int32_t *__restrict__ ids, int T, int K, int E, int tp
     // dst_row_fill: the chunk's slots start as kSlotPending, which the
     // kernel that ranks the chunk overwrites
     if (dst_row_fill)
-        for (int i = tid; i < m; i += kCountThreads) dst_row_fill[(size_t)t0 * K + i] = kSlotPending;
+        for (int i = tid; i < m; i += nthr) dst_row_fill[(size_t)t0 * K + i] = kSlotPending;
     stage_i32(ids_s, ids + (size_t)t0 * K, m);
     cp_async_wait_all();
     __syncthreads();
@@ -89,7 +88,7 @@ layout_count_kernel(const int32_t *__restrict__ ids, int T, int K, int E, int tp
     const bool groups = (32 % K) == 0;
     const unsigned group = K >= 32 ? kFullMask : (((1u << K) - 1u) << (lane - lane % K));
     uint32_t err = 0;
-    for (int b = tid - lane; b < m; b += kCountThreads) {
+    for (int b = tid - lane; b < m; b += nthr) {
         const int i = b + lane;
         const int id = i < m ? ids_s[i] : -1;
         const bool ok = (unsigned)id < (unsigned)E;
@@ -101,7 +100,7 @@ layout_count_kernel(const int32_t *__restrict__ ids, int T, int K, int E, int tp
     if (!groups) err |= token_errors(ids_s, t1 - t0, K, E);
     if (err) atomicOr(&s_err, err);
     __syncthreads();
-    for (int e = tid; e < E; e += kCountThreads) ws_cnt[(size_t)c * E + e] = hist[e];
+    for (int e = tid; e < E; e += nthr) ws_cnt[(size_t)c * E + e] = hist[e];
     if (tid == 0) ws_err[c] = s_err;
 }
 
@@ -330,12 +329,13 @@ WorkspaceLayout workspace_layout(int chunks, int E)
 cudaError_t launch_layout_count(const int32_t *topk_ids, int T, int K, int E,
                                 const LayoutPlan &p, int32_t *ws_cnt, uint32_t *ws_err,
                                 uint32_t *dev_error, int32_t *dst_row_fill,
-                                uint32_t *sync_zero, cudaStream_t stream)
+                                uint32_t *sync_zero, cudaStream_t stream, int threads)
 {
+    if (threads != 256 && threads != kCountThreads) return cudaErrorInvalidValue;
     const size_t csmem = sizeof(int32_t) * ((size_t)align4(E) + (size_t)p.tokens_per_chunk * K);
     cudaError_t e = allow_dynamic_smem((const void *)layout_count_kernel, csmem);
     if (e != cudaSuccess) return e;
-    return launch_pdl(layout_count_kernel, dim3(p.chunks), dim3(kCountThreads), csmem, stream,
+    return launch_pdl(layout_count_kernel, dim3(p.chunks), dim3(threads), csmem, stream,
                       topk_ids, T, K, E, p.tokens_per_chunk, p.chunks, ws_cnt, ws_err,
                       dev_error, dst_row_fill, sync_zero);
 }
@@ -356,6 +356,10 @@ cudaError_t launch_layout(const int32_t *topk_ids, int T, int K, int E, int R,
                           (const int32_t *)nullptr, expert_counts, expert_offsets,
                           rank_offsets, src_token, dst_row, dev_error);
     }
+    if (layout_ranked(T, K, E))
+        return launch_layout_ranked(topk_ids, T, K, E, R, expert_counts, expert_offsets,
+                                    rank_offsets, src_token, dst_row, dev_error, workspace,
+                                    stream);
     int32_t *ws_cnt = static_cast<int32_t *>(workspace);
     uint32_t *ws_err = reinterpret_cast<uint32_t *>(ws_cnt + (size_t)p.chunks * E);
     cudaError_t e = launch_layout_count(topk_ids, T, K, E, p, ws_cnt, ws_err, dev_error,

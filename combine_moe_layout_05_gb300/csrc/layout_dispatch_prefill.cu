@@ -50,6 +50,7 @@ constexpr size_t kMaxRankSmem = 24 * 1024;       // keeps packing blocks at full
 constexpr size_t kSmemPerSm = 228 * 1024;        // shared memory of one SM (sm_100 family)
 constexpr int kSmPerBlockLimit = 32;             // resident blocks per SM
 constexpr int kMaxRankBlocks = 128;              // ranking blocks resident together
+constexpr size_t kMaxRankOnlySmem = 96 * 1024;   // ranking blocks of moe_layout alone
 
 __device__ __forceinline__ uint64_t global_ns()
 {
@@ -429,6 +430,36 @@ rank_dispatch_kernel(const int32_t *__restrict__ ids, const uint4 *__restrict__ 
         store_to_slots<KT>(slots, k_count, rows, packed, vrow * 16, (size_t)rp.u * 16, a);
 }
 
+// The ranking blocks' plan: the layout's chunks, made larger where there
+// would be more than kMaxRankBlocks (fewer chunks also need less workspace
+// than the layout's plan), their shared memory, and whether the ranking
+// blocks' column step fits (each lane holds at most kColWords words).
+struct RankPlan {
+    bool ok;
+    LayoutPlan lp;
+    size_t smem;
+};
+
+RankPlan plan_rank(int T, int K, int E)
+{
+    RankPlan rp{};
+    rp.lp = plan_layout(T, K, E);
+    if (T <= 0 || rp.lp.single_launch) return rp;
+    // the ranking blocks wait for one another, so all of them must be
+    // resident at once
+    if (rp.lp.chunks > kMaxRankBlocks) {
+        rp.lp.tokens_per_chunk = ceil_div(T, kMaxRankBlocks);
+        rp.lp.chunks = ceil_div(T, rp.lp.tokens_per_chunk);
+    }
+    const int chunks = rp.lp.chunks;
+    const int ne_max = ceil_div(E, chunks);
+    rp.smem = sizeof(int32_t) * ((size_t)2 * align4(E) + align4(E + 1) + (size_t)kRankWarps * E +
+                                 align4(ne_max * chunks) + (size_t)rp.lp.tokens_per_chunk * K);
+    rp.ok = chunks <= 32 * kColWords &&
+            ne_max <= (kColWords >> (chunks <= 32 ? 0 : (chunks <= 64 ? 1 : 2))) * kRankWarps;
+    return rp;
+}
+
 struct PrefillPlan {
     bool use;
     LayoutPlan lp;          // this path's chunks (at most kMaxRankBlocks)
@@ -439,30 +470,19 @@ struct PrefillPlan {
 PrefillPlan plan_prefill(int T, int H, int K, int E, bool fp8)
 {
     PrefillPlan pp{};
-    pp.lp = plan_layout(T, K, E);
-    if (T <= 0 || pp.lp.single_launch) return pp;
-    // the ranking blocks wait for one another, so all of them must be
-    // resident at once: larger chunks where the layout's would be too many
-    // (fewer chunks also need less workspace than the layout's plan)
-    if (pp.lp.chunks > kMaxRankBlocks) {
-        pp.lp.tokens_per_chunk = ceil_div(T, kMaxRankBlocks);
-        pp.lp.chunks = ceil_div(T, pp.lp.tokens_per_chunk);
-    }
-    const int chunks = pp.lp.chunks;
+    const RankPlan rp = plan_rank(T, K, E);
+    pp.lp = rp.lp;
+    pp.smem = rp.smem;
+    if (!rp.ok) return pp;
     const int units = fp8 ? H / 16 : H / 8;
     pp.pack_blocks = ((long long)T * units + kRowThreads - 1) / kRowThreads;
-    const int ne_max = ceil_div(E, chunks);
-    pp.smem = sizeof(int32_t) * ((size_t)2 * align4(E) + align4(E + 1) + (size_t)kRankWarps * E +
-                                 align4(ne_max * chunks) + (size_t)pp.lp.tokens_per_chunk * K);
     // a packing block's tokens' slots, one per thread at most
     const long long max_slots = (long long)((units - 1 + kRowThreads - 1) / units + 1) * K;
-    const long long grid = (long long)chunks + pp.pack_blocks;
+    const long long grid = (long long)pp.lp.chunks + pp.pack_blocks;
     // every block carries the ranking blocks' shared memory: take this path
     // only while the packing blocks still fill at least 3/4 of an SM
     const long long per_sm = min((long long)kSmPerBlockLimit, (long long)(kSmemPerSm / (pp.smem + 1024)));
     pp.use = units < kMaxRowPieces && max_slots <= kRowThreads && pp.smem <= kMaxRankSmem &&
-             chunks <= 32 * kColWords &&
-             ne_max <= (kColWords >> (chunks <= 32 ? 0 : (chunks <= 64 ? 1 : 2))) * kRankWarps &&
              per_sm * kRowThreads >= 1536 && grid <= 0x7fffffffll;
     return pp;
 }
@@ -485,7 +505,7 @@ cudaError_t run_prefill(const PrefillPlan &pp, const int32_t *ids, const void *t
     auto *fn = rank_dispatch_kernel<KT, kFp8>;
     cudaError_t e = allow_dynamic_smem((const void *)fn, pp.smem);
     if (e != cudaSuccess) return e;
-    const unsigned grid = (unsigned)(pp.lp.chunks + pp.pack_blocks);
+    const unsigned grid = (unsigned)(pp.lp.chunks + pp.pack_blocks);   // no packing blocks: layout only
     return launch_pdl(fn, dim3(grid), dim3(kRowThreads), pp.smem, s, ids,
                       static_cast<const uint4 *>(tokens), T, H, K, E, R,
                       pp.lp.tokens_per_chunk, pp.lp.chunks, ws.cnt, ws.err, ws.tot, ws.sync,
@@ -523,6 +543,37 @@ bool layout_dispatch_prefill(int T, int H, int K, int E, int fp8)
     return plan_prefill(T, H, K, E, fp8 != 0).use;
 }
 
+bool layout_ranked(int T, int K, int E)
+{
+    const RankPlan rp = plan_rank(T, K, E);
+    return rp.ok && rp.smem <= kMaxRankOnlySmem;
+}
+
+cudaError_t launch_layout_ranked(const int32_t *topk_ids, int T, int K, int E, int R,
+                                 int32_t *expert_counts, int32_t *expert_offsets,
+                                 int32_t *rank_offsets, int32_t *src_token, int32_t *dst_row,
+                                 uint32_t *dev_error, void *workspace, cudaStream_t stream)
+{
+    const RankPlan rp = plan_rank(T, K, E);
+    if (!rp.ok || rp.smem > kMaxRankOnlySmem) return cudaErrorInvalidValue;
+    PrefillPlan pp{};
+    pp.use = true;
+    pp.lp = rp.lp;
+    pp.smem = rp.smem;
+    pp.pack_blocks = 0;                 // the grid is the ranking blocks alone
+    const WorkspaceLayout wl = workspace_layout(pp.lp.chunks, E);
+    int32_t *base = static_cast<int32_t *>(workspace);
+    const PrefillWorkspace ws{base, reinterpret_cast<uint32_t *>(base + wl.err), base + wl.tot,
+                              reinterpret_cast<uint32_t *>(base + wl.sync)};
+    // no packing blocks poll dst_row, so it needs no pending marks
+    cudaError_t e = launch_layout_count(topk_ids, T, K, E, pp.lp, ws.cnt, ws.err, dev_error,
+                                        nullptr, ws.sync, stream);
+    if (e != cudaSuccess) return e;
+    return run_prefill_k<false>(pp, topk_ids, nullptr, T, 8, K, E, R, ws, expert_counts,
+                                expert_offsets, rank_offsets, src_token, dst_row, dev_error,
+                                nullptr, nullptr, kWaitNs, -1, stream);
+}
+
 cudaError_t launch_layout_dispatch_prefill(const int32_t *topk_ids, const void *tokens, int T,
                                            int H, int K, int E, int R, int fp8,
                                            int32_t *expert_counts, int32_t *expert_offsets,
@@ -539,7 +590,7 @@ cudaError_t launch_layout_dispatch_prefill(const int32_t *topk_ids, const void *
     const PrefillWorkspace ws{base, reinterpret_cast<uint32_t *>(base + wl.err), base + wl.tot,
                               reinterpret_cast<uint32_t *>(base + wl.sync)};
     cudaError_t e = launch_layout_count(topk_ids, T, K, E, pp.lp, ws.cnt, ws.err, dev_error,
-                                        dst_row, ws.sync, stream);
+                                        dst_row, ws.sync, stream, 512);
     if (e != cudaSuccess) return e;
     if (wait_ns == 0) wait_ns = kWaitNs;
     if (fp8)

@@ -80,8 +80,10 @@ MOE_API const char *moe_status_string(moe_status_t status);
 MOE_API size_t moe_layout_workspace_bytes(int32_t T, int32_t K, int32_t E);
 
 /* Number of kernel launches moe_layout makes for these sizes: 1 when the
- * whole layout fits one launch of self-counting blocks, otherwise 3 (count,
- * scan, rank).  0 for invalid sizes.  A query: nothing is launched. */
+ * whole layout fits one launch of self-counting blocks, 2 (count, then
+ * ranking blocks that exchange the chunk histograms among themselves) when
+ * that plan fits, otherwise 3 (count, scan, rank; e.g. E near 1024).  0 for
+ * invalid sizes.  A query: nothing is launched. */
 MOE_API int32_t moe_layout_kernels(int32_t T, int32_t K, int32_t E);
 
 /*

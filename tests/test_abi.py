@@ -108,10 +108,12 @@ def test_layout_dispatch_plan_query(lib):
     assert moe.moe_layout_dispatch_kernels(1000, 4096, 8, 128, False) == 2
     assert moe.moe_layout_dispatch_kernels(5000, 65536, 8, 16, False) == 2
     assert moe.moe_layout_dispatch_kernels(2000, 1024, 8, 1024, False) == 4
-    # moe_layout alone: one self-counting launch, or count, scan, rank
+    # moe_layout alone: one self-counting launch, count + ranking blocks, or
+    # count, scan, rank
     assert moe.moe_layout_kernels(128, 8, 256) == 1
-    assert moe.moe_layout_kernels(4096, 8, 384) == 3
-    assert moe.moe_layout_kernels(16384, 8, 128) == 3
+    assert moe.moe_layout_kernels(4096, 8, 384) == 2                 # count + ranking
+    assert moe.moe_layout_kernels(16384, 8, 128) == 2
+    assert moe.moe_layout_kernels(2000, 8, 1024) == 3                # count, scan, rank
     assert moe.moe_layout_kernels(16384, 8, 100000) == 0             # invalid E
     assert moe.moe_layout_dispatch_kernels(512, 7168, 8, 256, False) == 2
     assert moe.moe_layout_dispatch_kernels(0, 128, 4, 16, False) == 1

@@ -135,4 +135,4 @@ def test_variant_options_and_launch_counts():
     assert bench.launches_per_step(q, "fp8", False, variant="persistent") == 3
     assert bench.launches_per_step(d, "bf16", False) == 2         # one fused kernel, combine
     assert bench.launches_per_step(d, "bf16", False, variant="cluster") == 2
-    assert bench.launches_per_step(q, "fp8", True) == 3 + 2       # count, scan, rank; dispatch; combine
+    assert bench.launches_per_step(q, "fp8", True) == 2 + 2       # count, ranking; dispatch; combine

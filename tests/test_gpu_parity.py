@@ -55,7 +55,7 @@ def test_layout_full_size(oracle, name):
     assert_layout_equal(buf, ref, w.T, w.K, w.E, w.R)
 
 
-SHAPES = [  # T, K, E, R: single kernel, count/scan/rank, ragged tails, limits
+SHAPES = [  # T, K, E, R: single kernel, count + ranking, count/scan/rank, ragged tails, limits
     (0, 4, 16, 4), (1, 1, 1, 1), (1, 8, 256, 32), (3, 2, 4, 2), (33, 3, 7, 7),
     (1000, 6, 64, 8), (1024, 8, 256, 32), (1025, 8, 256, 32),
     (1500, 5, 40, 5), (4097, 2, 1024, 16), (5000, 8, 1024, 1024),
@@ -68,7 +68,7 @@ SHAPES = [  # T, K, E, R: single kernel, count/scan/rank, ragged tails, limits
 
 
 def test_layout_shapes_cover_every_launch_plan():
-    assert {moe.moe_layout_kernels(T, K, E) for T, K, E, _ in SHAPES} == {1, 3}
+    assert {moe.moe_layout_kernels(T, K, E) for T, K, E, _ in SHAPES} == {1, 2, 3}
 
 
 @pytest.mark.parametrize("T,K,E,R", SHAPES)
