@@ -22,11 +22,14 @@
 //
 // Small batches (T*K <= kSelfMaxEntries) take one launch: each block stages
 // all T*K ids and counts the totals and the entries before its chunk itself.
-// Larger batches take three launches and a workspace, with no block ever
-// waiting for another: a counting kernel writes each chunk's histogram, a
-// one-block kernel turns the histograms into each chunk's first slot per
-// expert and writes the expert offsets, and the ranking kernel assigns the
-// slots.
+// Larger batches take a workspace and, where the ranking blocks' plan fits
+// (layout_ranked), two launches: this file's counting kernel, then the
+// ranking blocks of the large-batch layout + dispatch grid alone
+// (layout_dispatch_prefill.cu).  Otherwise (E near 1024) three, with no block
+// ever waiting for another: the counting kernel writes each chunk's
+// histogram, a one-block kernel turns the histograms into each chunk's first
+// slot per expert and writes the expert offsets, and the ranking kernel
+// assigns the slots.
 #include "common.cuh"
 #include "internal.h"
 #include "layout_common.cuh"
