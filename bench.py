@@ -183,7 +183,7 @@ def algorithmic_bytes(w, dispatch: str):
 # the sources each call's kernels are built from (their hash keys the DRAM
 # traffic rows in profiles/dram_traffic.json)
 CALL_SOURCES = {
-    "layout": ["layout.cu", "layout_common.cuh"],
+    "layout": ["layout.cu", "layout_common.cuh", "layout_dispatch_prefill.cu"],
     "dispatch": ["dispatch.cu", "rowops.cuh"],
     "combine": ["combine.cu", "combine_common.cuh"],
     "combine_fp8": ["combine_fp8.cu", "combine_common.cuh"],

@@ -206,13 +206,17 @@ __device__ __forceinline__ void rank_chunk(const int32_t *__restrict__ ids, int 
         s_ok = 1;
     }
     __syncthreads();
+    // The chunk's ids are an input of the call, complete before this grid
+    // started: the counting kernel's blocks let it start only after their own
+    // wait for the kernel before the call.  So they are staged before this
+    // grid's wait (which is for the counting kernel's histograms).
+    stage_i32(ids_s, ids + first, m);
     pdl_wait();
     pdl_trigger();
-    stage_i32(ids_s, ids + first, m);
 
-    // 1. this warp's histogram words, requested together with the chunk's
-    //    ids (word k: column w + (k >> lp) * kRankWarps, chunk q0 + k % 2^lp);
-    //    then the ranks within each warp's segment; then the columns' prefixes
+    // 1. this warp's histogram words (word k: column w + (k >> lp) *
+    //    kRankWarps, chunk q0 + k % 2^lp), then the ranks within each warp's
+    //    segment; then the columns' prefixes
     {
         int32_t hv[kColWords];
 #pragma unroll
