@@ -150,17 +150,19 @@ __device__ __forceinline__ void warp_local_rank(int32_t *ids, int lo, int hi, in
 
 // Block c (< chunks) of rank_dispatch_kernel: ranks chunk c and publishes it.
 //
+//  0. Before the grid's wait (the ids are an input of the call, complete
+//     when the grid starts) it stages the chunk's ids, ranks each entry
+//     among the equal ids of its warp's segment and turns the per-warp
+//     counts into per-warp starts.
 //  1. The block owns expert columns [e0, e0 + ne) of the chunk histograms
 //     (ne = ceil(E / chunks)); its warps turn them into their exclusive
-//     prefix over the chunks, in place, and write the column totals to
-//     ws_tot.  Every histogram word is read by one block only.  While those
-//     words are in flight the block ranks each entry of its own chunk among
-//     the equal ids of its warp's segment.
+//     prefix over the chunks, in place, from the words each lane holds in
+//     registers, and write the column totals to ws_tot.  Every histogram
+//     word is read by one block only.
 //  2. It announces step 1 on the arrival counter (zeroed by the counting
-//     kernel), turns the per-warp counts into per-warp starts, and waits
-//     (bounded) until every ranking block has arrived.  The ranking blocks
-//     are the first blocks of the grid and at most kMaxRankBlocks, so they
-//     are resident together.
+//     kernel) and waits (bounded) until every ranking block has arrived.
+//     The ranking blocks are the first blocks of the grid and at most
+//     kMaxRankBlocks, so they are resident together.
 //  3. It reads the totals and its chunk's row of prefixes, scans the totals
 //     into expert_offsets and writes every entry's slot,
 //         offsets[e] + prefix[c][e] + (warp's start for e) + rank in warp,
@@ -185,8 +187,7 @@ __device__ __forceinline__ void rank_chunk(const int32_t *__restrict__ ids, int 
     int32_t *pre = tot + align4(E);              // [E]
     int32_t *base = pre + align4(E);             // [E + 1]
     int32_t *cnt = base + align4(E + 1);         // [kRankWarps][E], 16-byte aligned
-    int32_t *col = cnt + E * kRankWarps;         // [ne][chunks]
-    int32_t *ids_s = col + align4(ceil_div(E, chunks) * chunks);   // [tpc * K], 16-byte aligned
+    int32_t *ids_s = cnt + E * kRankWarps;       // [tpc * K], 16-byte aligned
     __shared__ int32_t warp_sums[32];
     __shared__ uint32_t s_err;
     __shared__ int s_ok;
@@ -205,65 +206,18 @@ __device__ __forceinline__ void rank_chunk(const int32_t *__restrict__ ids, int 
         s_err = 0;
         s_ok = 1;
     }
-    __syncthreads();
     // The chunk's ids are an input of the call, complete before this grid
     // started: the counting kernel's blocks let it start only after their own
-    // wait for the kernel before the call.  So they are staged before this
-    // grid's wait (which is for the counting kernel's histograms).
+    // wait for the kernel before the call.  So they are staged and ranked,
+    // and the warps' starts computed, before this grid's wait, which is for
+    // the counting kernel's histograms only.
     stage_i32(ids_s, ids + first, m);
-    pdl_wait();
-    pdl_trigger();
-
-    // 1. this warp's histogram words (word k: column w + (k >> lp) *
-    //    kRankWarps, chunk q0 + k % 2^lp), then the ranks within each warp's
-    //    segment; then the columns' prefixes
-    {
-        int32_t hv[kColWords];
-#pragma unroll
-        for (int k = 0; k < kColWords; ++k) {
-            const int j = w + (k >> lp) * kRankWarps, q = q0 + (k & ((1 << lp) - 1));
-            hv[k] = j < ne && q < chunks ? ld_l2(ws_cnt + (size_t)q * E + e0 + j) : 0;
-        }
-        cp_async_wait_all();
-#pragma unroll
-        for (int k = 0; k < kColWords; ++k) {
-            const int j = w + (k >> lp) * kRankWarps, q = q0 + (k & ((1 << lp) - 1));
-            if (j < ne && q < chunks) col[j * chunks + q] = hv[k];
-        }
-    }
-    if (c == 0) {
-        uint32_t err = 0;
-        for (int q = tid; q < chunks; q += nthr) err |= ld_relaxed(ws_err + q) & ~kAbandonedBit;
-        if (err) atomicOr(&s_err, err);
-    }
+    cp_async_wait_all();
+    __syncthreads();
     const int seg = ((m + kRankWarps - 1) / kRankWarps + 31) & ~31;
     const int lo = min(m, w * seg), hi = min(m, lo + seg);
-    __syncthreads();
     warp_local_rank(ids_s, lo, hi, E, lane, cnt + w * E);
-    for (int j = w; j < ne; j += kRankWarps) {
-        const int32_t *cj = col + j * chunks;
-        const int q1 = min(chunks, q0 + (1 << lp));
-        int sum = 0;
-        for (int q = q0; q < q1; ++q) sum += cj[q];
-        int x = sum;
-#pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-            const int y = __shfl_up_sync(kFullMask, x, d);
-            if (lane >= d) x += y;
-        }
-        int run = x - sum;
-        for (int q = q0; q < q1; ++q) {
-            ws_cnt[(size_t)q * E + e0 + j] = run;
-            run += cj[q];
-        }
-        if (lane == 31) ws_tot[e0 + j] = x;
-    }
-
-    // 2. arrive; per-warp starts while the others arrive; wait for them
-    __threadfence();
     __syncthreads();
-    if (c == -2 - stall_chunk) return;      // test hook: this block never arrives
-    if (tid == 0) atomicAdd(ws_sync, 1u);
     for (int e = tid; e < E; e += nthr) {
         int32_t v[kRankWarps];
 #pragma unroll
@@ -275,7 +229,55 @@ __device__ __forceinline__ void rank_chunk(const int32_t *__restrict__ ids, int 
             run += v[ww];
         }
     }
+    pdl_wait();
+    pdl_trigger();
+
+    // 1. this warp's histogram words (word k: column w + (k >> lp) *
+    //    kRankWarps, chunk q0 + k % 2^lp), then each column's prefix over
+    //    the chunks
+    int32_t hv[kColWords];
+#pragma unroll
+    for (int k = 0; k < kColWords; ++k) {
+        const int j = w + (k >> lp) * kRankWarps, q = q0 + (k & ((1 << lp) - 1));
+        hv[k] = j < ne && q < chunks ? ld_l2(ws_cnt + (size_t)q * E + e0 + j) : 0;
+    }
+    if (c == 0) {
+        uint32_t err = 0;
+        for (int q = tid; q < chunks; q += nthr) err |= ld_relaxed(ws_err + q) & ~kAbandonedBit;
+        if (err) atomicOr(&s_err, err);
+    }
+#pragma unroll
+    for (int i = 0; i < kColWords; ++i) {
+        const int j = w + i * kRankWarps;
+        if ((i << lp) >= kColWords || j >= ne) break;
+        int sum = 0;
+#pragma unroll
+        for (int k = 0; k < kColWords; ++k)
+            if ((k >> lp) == i) sum += hv[k];
+        int x = sum;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int y = __shfl_up_sync(kFullMask, x, d);
+            if (lane >= d) x += y;
+        }
+        int run = x - sum;
+#pragma unroll
+        for (int k = 0; k < kColWords; ++k) {
+            const int q = q0 + (k & ((1 << lp) - 1));
+            if ((k >> lp) == i && q < chunks) {
+                ws_cnt[(size_t)q * E + e0 + j] = run;
+                run += hv[k];
+            }
+        }
+        if (lane == 31) ws_tot[e0 + j] = x;
+    }
+
+    // 2. arrive, and wait for the other ranking blocks
+    __threadfence();
+    __syncthreads();
+    if (c == -2 - stall_chunk) return;      // test hook: this block never arrives
     if (tid == 0) {
+        atomicAdd(ws_sync, 1u);
         const unsigned long long deadline = global_ns() + wait_ns;
         while (ld_relaxed(ws_sync) < (uint32_t)chunks) {
             __nanosleep(32);
@@ -297,9 +299,10 @@ __device__ __forceinline__ void rank_chunk(const int32_t *__restrict__ ids, int 
     }
 
     // 3. expert offsets, then every entry's slot
+    // (chunk 0's prefixes are all zero)
     for (int e = tid; e < E; e += nthr) {
         tot[e] = ld_l2(ws_tot + e);
-        pre[e] = ld_l2(ws_cnt + (size_t)c * E + e);
+        if (c) pre[e] = ld_l2(ws_cnt + (size_t)c * E + e);
     }
     __syncthreads();
     block_scan(tot, base, E, warp_sums);
@@ -314,10 +317,10 @@ __device__ __forceinline__ void rank_chunk(const int32_t *__restrict__ ids, int 
         }
         const int epr = E / R;
         for (int r = tid; r <= R; r += nthr) rank_offsets[r] = base[r * epr];
+    } else {
+        for (int e = tid; e < E; e += nthr) base[e] += pre[e];
+        __syncthreads();
     }
-    __syncthreads();
-    for (int e = tid; e < E; e += nthr) base[e] += pre[e];
-    __syncthreads();
     if (c == stall_chunk) return;           // test hook: the chunk's slots stay pending
     for (int i = lo + lane; i < hi; i += 32) {
         const int v = ids_s[i];
@@ -458,7 +461,7 @@ RankPlan plan_rank(int T, int K, int E)
     const int chunks = rp.lp.chunks;
     const int ne_max = ceil_div(E, chunks);
     rp.smem = sizeof(int32_t) * ((size_t)2 * align4(E) + align4(E + 1) + (size_t)kRankWarps * E +
-                                 align4(ne_max * chunks) + (size_t)rp.lp.tokens_per_chunk * K);
+                                 (size_t)rp.lp.tokens_per_chunk * K);
     rp.ok = chunks <= 32 * kColWords &&
             ne_max <= (kColWords >> (chunks <= 32 ? 0 : (chunks <= 64 ? 1 : 2))) * kRankWarps;
     return rp;
