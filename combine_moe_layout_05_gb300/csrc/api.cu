@@ -57,7 +57,7 @@ const char *moe_status_string(moe_status_t status)
 size_t moe_layout_workspace_bytes(int32_t T, int32_t K, int32_t E)
 {
     if (!layout_sizes_ok(T, K, E)) return 0;
-    return moe::layout_workspace_bytes(moe::plan_layout(T, K, E), E);
+    return moe::layout_workspace_bytes(T, K, E);
 }
 
 moe_status_t moe_layout(const int32_t *topk_ids, int32_t T, int32_t K,
@@ -75,7 +75,7 @@ moe_status_t moe_layout(const int32_t *topk_ids, int32_t T, int32_t K,
                         src_token, dst_row, dev_error};
     for (const void *p : p4)
         if (!aligned(p, 4)) return MOE_ERR_ALIGNMENT;
-    const size_t need = moe::layout_workspace_bytes(moe::plan_layout(T, K, E), E);
+    const size_t need = moe::layout_workspace_bytes(T, K, E);
     if (need > 0) {
         if (!workspace || workspace_bytes < need) return MOE_ERR_WORKSPACE;
         if (!aligned(workspace, 16)) return MOE_ERR_ALIGNMENT;
@@ -235,7 +235,7 @@ moe_status_t moe_layout_dispatch(const int32_t *topk_ids, const void *tokens,
         if (!aligned(p, 4)) return MOE_ERR_ALIGNMENT;
     if (!aligned(tokens, 16) || !aligned(packed, 16)) return MOE_ERR_ALIGNMENT;
     if (!moe::layout_dispatch_fused(T, H, K, fp8)) {
-        const size_t need = moe::layout_workspace_bytes(moe::plan_layout(T, K, E), E);
+        const size_t need = moe::layout_workspace_bytes(T, K, E);
         if (need > 0) {
             if (!workspace || workspace_bytes < need) return MOE_ERR_WORKSPACE;
             if (!aligned(workspace, 16)) return MOE_ERR_ALIGNMENT;

@@ -18,31 +18,44 @@ struct LayoutPlan {
 LayoutPlan plan_layout(int T, int K, int E);
 // False when a batch this large would not fit the kernels' shared memory.
 bool layout_supported(int T, int K, int E);
-size_t layout_workspace_bytes(const LayoutPlan &plan, int E);
+// Bytes of workspace moe_layout and moe_layout_dispatch need for these sizes:
+// the larger of the count/scan/rank form's and the ranking blocks' form's.
+size_t layout_workspace_bytes(int T, int K, int E);
 
-// Where the multi-block layouts keep their state in the workspace, in int32
-// elements from its start: ws_cnt[chunks][E] (chunk histograms), then
-// ws_err[chunks] (chunk error bits), ws_tot[E] (expert totals) and one
-// arrival counter.
+// Where the count/scan/rank layout keeps its state in the workspace, in
+// int32 elements from its start: ws_cnt[chunks][E] (chunk histograms, then
+// each chunk's first slot per expert), then ws_err[chunks] (chunk error
+// bits).
 struct WorkspaceLayout {
-    size_t err, tot, sync;   // element offsets
+    size_t err;              // element offset
     size_t bytes;            // bytes used
 };
 WorkspaceLayout workspace_layout(int chunks, int E);
 
-// The counting kernel of the multi-launch layout alone: chunk histograms to
-// ws_cnt[chunks][E], chunk error bits to ws_err[chunks], dev_error zeroed,
-// when dst_row_fill is not null every dst_row entry set to kSlotPending, and
-// and when sync_zero is not null that word zeroed.  threads: 256 or 512 per
-// block (one chunk per block).  512 measured 0.2-0.4 us faster inside the
-// large-batch moe_layout_dispatch at Kimi-K2 sizes (equal at Qwen3), but
+// Blocks per thread-block cluster of the counting kernel in its clustered
+// form (the largest portable cluster).
+constexpr int kCountCluster = 8;
+
+// The counting kernel of the multi-launch layout alone: chunk error bits to
+// ws_err[chunks], dev_error zeroed, and when dst_row_fill is not null every
+// dst_row entry set to kSlotPending.  With ws_ctot null it writes each
+// chunk's histogram to ws_cnt[chunks][E].  With ws_ctot set it runs in
+// clusters of kCountCluster blocks (chunks kCountCluster*g .. +7 form
+// cluster g; the grid is padded with empty chunks) and writes, through
+// distributed shared memory, each chunk's exclusive prefix within its
+// cluster, ws_cnt[c][e] = entries of e in the earlier chunks of c's
+// cluster, and each cluster's totals, ws_ctot[g][e], both in rows of
+// align4(E) elements.  threads: 256 or 512
+// per block (one chunk per block).  512 measured 0.2-0.4 us faster inside
+// the large-batch moe_layout_dispatch at Kimi-K2 sizes (equal at Qwen3), but
 // 5 us slower ahead of moe_layout's ranking-only grid at Qwen3 sizes, where
 // 256 is used.
 constexpr int32_t kSlotPending = INT32_MIN;
 cudaError_t launch_layout_count(const int32_t *topk_ids, int T, int K, int E,
                                 const LayoutPlan &plan, int32_t *ws_cnt, uint32_t *ws_err,
                                 uint32_t *dev_error, int32_t *dst_row_fill,
-                                uint32_t *sync_zero, cudaStream_t stream, int threads = 256);
+                                cudaStream_t stream, int threads = 256,
+                                int32_t *ws_ctot = nullptr);
 
 cudaError_t launch_layout(const int32_t *topk_ids, int T, int K, int E, int R,
                           int32_t *expert_counts, int32_t *expert_offsets,
@@ -156,6 +169,8 @@ cudaError_t launch_layout_dispatch_prefill(const int32_t *topk_ids, const void *
 // layout + dispatch grid alone.  layout_ranked() says whether these sizes take
 // it; otherwise launch_layout runs count, scan and rank.
 bool layout_ranked(int T, int K, int E);
+// Workspace bytes of the ranking blocks' form (0 when it does not apply).
+size_t ranked_workspace_bytes(int T, int K, int E);
 cudaError_t launch_layout_ranked(const int32_t *topk_ids, int T, int K, int E, int R,
                                  int32_t *expert_counts, int32_t *expert_offsets,
                                  int32_t *rank_offsets, int32_t *src_token, int32_t *dst_row,

@@ -23,17 +23,22 @@
 // Small batches (T*K <= kSelfMaxEntries) take one launch: each block stages
 // all T*K ids and counts the totals and the entries before its chunk itself.
 // Larger batches take a workspace and, where the ranking blocks' plan fits
-// (layout_ranked), two launches: this file's counting kernel, then the
-// ranking blocks of the large-batch layout + dispatch grid alone
-// (layout_dispatch_prefill.cu).  Otherwise (E near 1024) three, with no block
-// ever waiting for another: the counting kernel writes each chunk's
-// histogram, a one-block kernel turns the histograms into each chunk's first
-// slot per expert and writes the expert offsets, and the ranking kernel
-// assigns the slots.
+// (layout_ranked), two launches: this file's counting kernel in clusters of
+// blocks, which sum their histograms through distributed shared memory,
+// then the ranking blocks of the large-batch layout + dispatch grid alone
+// (layout_dispatch_prefill.cu).  Otherwise (large batches with E near 1024)
+// three: the counting kernel writes each chunk's histogram, a one-block
+// kernel turns the histograms into each chunk's first slot per expert and
+// writes the expert offsets, and the ranking kernel assigns the slots.  In
+// no form does a block wait for another block of its own grid.
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 #include "internal.h"
 #include "layout_common.cuh"
 #include "moe_layout.h"
+
+namespace cg = cooperative_groups;
 
 namespace moe {
 namespace {
@@ -50,16 +55,18 @@ constexpr int kScanCells = 16 * 1024;    // chunks x E staged by the scan (64 KB
 constexpr int kScanThreads = 1024;
 
 // Multi-launch path, kernel 1: histogram and error bits of chunk c.
-// ws_cnt is chunk-major: ws_cnt[c * E + e].  Each warp takes 32 entries at a
+// ws_cnt is chunk-major: ws_cnt[c * E + e] (the clustered form writes
+// prefixes within each cluster there instead, see below).  Each warp takes 32 entries at a
 // time and matches equal ids, so one lane adds each distinct id's count (a
 // hot expert costs one shared atomic per warp step, not one per entry); when
 // K divides 32 the tokens' entries are whole lane groups and the same match
 // shows a duplicated id within a token.
+template <bool kCluster>
 __global__ void __launch_bounds__(kCountThreads)
 layout_count_kernel(const int32_t *__restrict__ ids, int T, int K, int E, int tpc,
                     int chunks, int32_t *__restrict__ ws_cnt,
                     uint32_t *__restrict__ ws_err, uint32_t *__restrict__ dev_error,
-                    int32_t *__restrict__ dst_row_fill, uint32_t *__restrict__ sync_zero)
+                    int32_t *__restrict__ dst_row_fill, int32_t *__restrict__ ws_ctot)
 {
     extern __shared__ __align__(16) int32_t sm[];
     int32_t *hist = sm;                      // [E]
@@ -76,10 +83,7 @@ layout_count_kernel(const int32_t *__restrict__ ids, int T, int K, int E, int tp
     pdl_wait();
     pdl_trigger();
     // the error word starts at zero; the kernels after this one OR into it
-    if (c == 0 && tid == 0) {
-        if (dev_error) *dev_error = 0;
-        if (sync_zero) *sync_zero = 0;
-    }
+    if (c == 0 && tid == 0 && dev_error) *dev_error = 0;
     // dst_row_fill: the chunk's slots start as kSlotPending, which the
     // kernel that ranks the chunk overwrites
     if (dst_row_fill)
@@ -102,9 +106,44 @@ layout_count_kernel(const int32_t *__restrict__ ids, int T, int K, int E, int tp
     }
     if (!groups) err |= token_errors(ids_s, t1 - t0, K, E);
     if (err) atomicOr(&s_err, err);
-    __syncthreads();
-    for (int e = tid; e < E; e += nthr) ws_cnt[(size_t)c * E + e] = hist[e];
-    if (tid == 0) ws_err[c] = s_err;
+    if constexpr (!kCluster) {
+        __syncthreads();
+        for (int e = tid; e < E; e += nthr) ws_cnt[(size_t)c * E + e] = hist[e];
+        if (tid == 0) ws_err[c] = s_err;
+    } else {
+        // Clustered form: block r of cluster g takes the expert slice
+        // [r * es, (r + 1) * es) of the cluster's kCountCluster histograms,
+        // read from the other blocks' shared memory.  Lane j of each group of
+        // kCountCluster lanes holds chunk kCountCluster * g + j of one expert;
+        // a scan across the group gives the chunk's prefix within the cluster,
+        // and the group's last lane the cluster's total.
+        cg::cluster_group cluster = cg::this_cluster();
+        cluster.sync();                      // every histogram of the cluster is complete
+        if (tid == 0 && c < chunks) ws_err[c] = s_err;
+        const int r = (int)cluster.block_rank(), g = c / kCountCluster;
+        const int j = tid % kCountCluster;
+        const int es = ceil_div(E, kCountCluster);
+        const int e_lo = min(E, r * es), n = (min(E, e_lo + es) - e_lo) * kCountCluster;
+        const int32_t *peer = cluster.map_shared_rank(hist, j);
+        const int q = g * kCountCluster + j;
+        const size_t ep = (size_t)align4(E);     // row stride: rows start 16-byte aligned
+        for (int b = 0; b < n; b += nthr) {  // whole warps take the shuffles
+            const int i = b + tid;
+            const int e = e_lo + i / kCountCluster;
+            const int v = i < n ? peer[e] : 0;
+            int x = v;
+#pragma unroll
+            for (int d = 1; d < kCountCluster; d <<= 1) {
+                const int y = __shfl_up_sync(kFullMask, x, d, kCountCluster);
+                if (j >= d) x += y;
+            }
+            if (i < n) {
+                if (q < chunks) ws_cnt[q * ep + e] = x - v;
+                if (j == kCountCluster - 1) ws_ctot[g * ep + e] = x;
+            }
+        }
+        cluster.sync();                      // no block leaves while its histogram is read
+    }
 }
 
 // Multi-launch path, kernel 2 (one block): turns the chunk histograms into
@@ -312,35 +351,45 @@ bool layout_supported(int T, int K, int E)
     return count <= kLimit && scan <= kLimit;
 }
 
-size_t layout_workspace_bytes(const LayoutPlan &plan, int E)
+size_t layout_workspace_bytes(int T, int K, int E)
 {
+    const LayoutPlan plan = plan_layout(T, K, E);
     if (plan.single_launch) return 0;
-    const WorkspaceLayout w = workspace_layout(plan.chunks, E);
-    return (w.bytes + 255) & ~(size_t)255;
+    size_t bytes = workspace_layout(plan.chunks, E).bytes;
+    const size_t ranked = ranked_workspace_bytes(T, K, E);
+    if (ranked > bytes) bytes = ranked;
+    return (bytes + 255) & ~(size_t)255;
 }
 
 WorkspaceLayout workspace_layout(int chunks, int E)
 {
     WorkspaceLayout w;
     w.err = (size_t)chunks * E;
-    w.tot = w.err + (size_t)chunks;
-    w.sync = w.tot + (size_t)E;
-    w.bytes = sizeof(int32_t) * (w.sync + 1);
+    w.bytes = sizeof(int32_t) * (w.err + (size_t)chunks);
     return w;
 }
 
 cudaError_t launch_layout_count(const int32_t *topk_ids, int T, int K, int E,
                                 const LayoutPlan &p, int32_t *ws_cnt, uint32_t *ws_err,
                                 uint32_t *dev_error, int32_t *dst_row_fill,
-                                uint32_t *sync_zero, cudaStream_t stream, int threads)
+                                cudaStream_t stream, int threads, int32_t *ws_ctot)
 {
     if (threads != 256 && threads != kCountThreads) return cudaErrorInvalidValue;
     const size_t csmem = sizeof(int32_t) * ((size_t)align4(E) + (size_t)p.tokens_per_chunk * K);
-    cudaError_t e = allow_dynamic_smem((const void *)layout_count_kernel, csmem);
+    if (ws_ctot) {
+        const unsigned grid = (unsigned)(ceil_div(p.chunks, kCountCluster) * kCountCluster);
+        cudaError_t e = allow_dynamic_smem((const void *)layout_count_kernel<true>, csmem);
+        if (e != cudaSuccess) return e;
+        return launch_pdl_clusters(layout_count_kernel<true>, dim3(grid), dim3(threads), csmem,
+                                   stream, (unsigned)kCountCluster, topk_ids, T, K, E,
+                                   p.tokens_per_chunk, p.chunks, ws_cnt, ws_err, dev_error,
+                                   dst_row_fill, ws_ctot);
+    }
+    cudaError_t e = allow_dynamic_smem((const void *)layout_count_kernel<false>, csmem);
     if (e != cudaSuccess) return e;
-    return launch_pdl(layout_count_kernel, dim3(p.chunks), dim3(threads), csmem, stream,
+    return launch_pdl(layout_count_kernel<false>, dim3(p.chunks), dim3(threads), csmem, stream,
                       topk_ids, T, K, E, p.tokens_per_chunk, p.chunks, ws_cnt, ws_err,
-                      dev_error, dst_row_fill, sync_zero);
+                      dev_error, dst_row_fill, (int32_t *)nullptr);
 }
 
 cudaError_t launch_layout(const int32_t *topk_ids, int T, int K, int E, int R,
@@ -366,7 +415,7 @@ cudaError_t launch_layout(const int32_t *topk_ids, int T, int K, int E, int R,
     int32_t *ws_cnt = static_cast<int32_t *>(workspace);
     uint32_t *ws_err = reinterpret_cast<uint32_t *>(ws_cnt + (size_t)p.chunks * E);
     cudaError_t e = launch_layout_count(topk_ids, T, K, E, p, ws_cnt, ws_err, dev_error,
-                                        nullptr, nullptr, stream);
+                                        nullptr, stream);
     if (e != cudaSuccess) return e;
     const size_t ssmem = sizeof(int32_t) * (size_t)E * p.chunks;
     e = allow_dynamic_smem((const void *)layout_scan_kernel, ssmem);

@@ -418,7 +418,7 @@ cudaError_t launch_layout_dispatch_persistent(const int32_t *topk_ids, const voi
     int32_t *ws_cnt = static_cast<int32_t *>(workspace);
     uint32_t *ws_err = reinterpret_cast<uint32_t *>(ws_cnt + (size_t)lp.chunks * E);
     cudaError_t e = launch_layout_count(topk_ids, T, K, E, lp, ws_cnt, ws_err, dev_error,
-                                        nullptr, nullptr, stream);
+                                        nullptr, stream);
     if (e != cudaSuccess) return e;
     if (wait_ns == 0) wait_ns = kWaitNs;
 #define MOE_PACK_ARGS                                                                     \

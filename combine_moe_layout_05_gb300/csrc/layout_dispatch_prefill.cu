@@ -9,15 +9,18 @@
 // HBM-bound copy of hundreds of megabytes; what the layout adds is latency
 // in front of it, which this path hides under the copy's own reads:
 //
-//  * layout_count_kernel (layout.cu) writes each chunk's histogram and error
-//    bits to the workspace, sets every dst_row entry to kSlotPending and
-//    zeroes the error word and the ranking blocks' arrival counter;
+//  * layout_count_kernel (layout.cu), in clusters of kCountCluster blocks,
+//    counts each chunk's experts and, through distributed shared memory,
+//    writes each chunk's prefix within its cluster and each cluster's
+//    totals to the workspace, with the chunks' error bits; it sets every
+//    dst_row entry to kSlotPending and zeroes the error word;
 //  * rank_dispatch_kernel: its first C blocks (C <= kMaxRankBlocks) each
-//    rank one chunk of tokens.  Together they turn the histograms into
-//    per-chunk exclusive prefixes and per-expert totals (each block scans a
-//    slice of the expert columns), meet at an arrival counter, and then
-//    block c scans the totals into expert_offsets and writes the dst_row and
-//    src_token entries of its chunk in the same stable order as moe_layout.
+//    rank one chunk of tokens.  A ranking block ranks its chunk's entries
+//    (from the ids alone) before its wait for the counting kernel; then it
+//    reads the clusters' totals and its chunk's prefix in one round of
+//    copies, scans the totals into expert_offsets and writes the dst_row
+//    and src_token entries of its chunk in the same stable order as
+//    moe_layout.  No ranking block waits for another.
 //    Every other block packs 256 consecutive 16-byte pieces of the flat
 //    sequence of all token rows, like moe_dispatch: its first threads read
 //    the K slots of each token it touches while all of them load their
@@ -30,11 +33,10 @@
 //
 // The ranking blocks come first in the grid, so they are scheduled before
 // any packing block that waits for them.  Each wait is bounded: past its
-// deadline a ranking block marks its chunk abandoned in the workspace, and a
-// packing block marks the chunk of the slot it waited for (so the chunk's
-// other blocks stop waiting at once); either sets MOE_DEV_ERR_TIMEOUT in the
-// error word, and the rows of the slots that could not be read stay
-// unwritten.
+// deadline a packing block marks the chunk of the slot it waited for
+// abandoned in the workspace (so the chunk's other blocks stop waiting at
+// once) and sets MOE_DEV_ERR_TIMEOUT in the error word; the rows of the
+// slots that could not be read stay unwritten.
 #include "common.cuh"
 #include "internal.h"
 #include "layout_common.cuh"
@@ -46,10 +48,14 @@ namespace {
 
 constexpr uint32_t kAbandonedBit = 0x80000000u;  // ws_err[c]: a wait for chunk c expired
 constexpr unsigned long long kWaitNs = 1000000000ull;   // 1 s
-constexpr size_t kMaxRankSmem = 24 * 1024;       // keeps packing blocks at full occupancy
+constexpr size_t kMaxRankSmem = 28 * 1024;       // keeps packing blocks at full occupancy
 constexpr size_t kSmemPerSm = 228 * 1024;        // shared memory of one SM (sm_100 family)
 constexpr int kSmPerBlockLimit = 32;             // resident blocks per SM
-constexpr int kMaxRankBlocks = 128;              // ranking blocks resident together
+constexpr int kMaxRankBlocks = 128;              // ranking blocks (chunks) per grid
+// moe_layout's ranking-only grid: measured 7.7 us at Qwen3 prefill sizes
+// with 64 chunks against 10.2 with 128 (and 10.6 with 32); with packing
+// blocks behind them 128 stays the fastest
+constexpr int kMaxRankOnlyBlocks = 64;
 constexpr size_t kMaxRankOnlySmem = 96 * 1024;   // ranking blocks of moe_layout alone
 
 __device__ __forceinline__ uint64_t global_ns()
@@ -118,13 +124,9 @@ __device__ __forceinline__ void block_scan(const int32_t *hist, int32_t *off, in
     __syncthreads();
 }
 
-// Loads of workspace words that other blocks of this grid write (second-
-// level cache only, so no stale first-level line is seen).
-__device__ __forceinline__ int32_t ld_l2(const int32_t *p) { return __ldcg(p); }
 
 constexpr int kIdBits = 11;               // ids below 2^11 > MOE_MAX_EXPERTS
 constexpr int kRankWarps = kRowThreads / 32;
-constexpr int kColWords = 4;              // histogram words per lane in step 1
 
 // Stable rank of each valid entry of ids[lo, hi) among the equal ids of this
 // warp's segment, 32 entries at a time (a warp match gives the lanes with
@@ -148,64 +150,62 @@ __device__ __forceinline__ void warp_local_rank(int32_t *ids, int lo, int hi, in
     }
 }
 
+// Shared memory of a ranking block, in int32 elements: the clusters' totals
+// [clusters][E] (row 0 becomes the expert totals), the chunk's prefix row
+// [E], the offsets [E + 1], the per-warp counters [kRankWarps][E] and the
+// chunk's ids.
+__host__ __device__ inline size_t rank_smem_words(int chunks, int tpc, int K, int E)
+{
+    const int nc = (chunks + kCountCluster - 1) / kCountCluster;
+    return (size_t)nc * align4(E) + align4(E) + align4(E + 1) + (size_t)kRankWarps * E +
+           (size_t)tpc * K;
+}
+
 // Block c (< chunks) of rank_dispatch_kernel: ranks chunk c and publishes it.
 //
 //  0. Before the grid's wait (the ids are an input of the call, complete
 //     when the grid starts) it stages the chunk's ids, ranks each entry
 //     among the equal ids of its warp's segment and turns the per-warp
 //     counts into per-warp starts.
-//  1. The block owns expert columns [e0, e0 + ne) of the chunk histograms
-//     (ne = ceil(E / chunks)); its warps turn them into their exclusive
-//     prefix over the chunks, in place, from the words each lane holds in
-//     registers, and write the column totals to ws_tot.  Every histogram
-//     word is read by one block only.
-//  2. It announces step 1 on the arrival counter (zeroed by the counting
-//     kernel) and waits (bounded) until every ranking block has arrived.
-//     The ranking blocks are the first blocks of the grid and at most
-//     kMaxRankBlocks, so they are resident together.
-//  3. It reads the totals and its chunk's row of prefixes, scans the totals
-//     into expert_offsets and writes every entry's slot,
-//         offsets[e] + prefix[c][e] + (warp's start for e) + rank in warp,
-//     each entry on its own.
+//  1. After the wait (for the counting kernel, which ran in clusters of
+//     kCountCluster chunks) it copies every cluster's totals and its chunk's
+//     prefix within its own cluster to shared memory, in one round of
+//     copies, and sums them into each expert's total and each expert's
+//     entries in the chunks before this one.
+//  2. It scans the totals into expert_offsets and writes every entry's slot,
+//         offsets[e] + (entries of e in earlier chunks)
+//                    + (warp's start for e) + rank in warp,
+//     each entry on its own.  No ranking block waits for another.
 __device__ __forceinline__ void rank_chunk(const int32_t *__restrict__ ids, int T, int K, int E,
                                         int R, int tpc, int chunks, int c,
-                                        int32_t *__restrict__ ws_cnt,
-                                        uint32_t *__restrict__ ws_err,
-                                        int32_t *__restrict__ ws_tot,
-                                        uint32_t *__restrict__ ws_sync,
+                                        const int32_t *__restrict__ ws_pre,
+                                        const uint32_t *__restrict__ ws_err,
+                                        const int32_t *__restrict__ ws_ctot,
                                         int32_t *__restrict__ counts,
                                         int32_t *__restrict__ offsets,
                                         int32_t *__restrict__ rank_offsets,
                                         int32_t *__restrict__ src_token,
                                         int32_t *__restrict__ dst_row,
-                                        uint32_t *__restrict__ dev_error,
-                                        unsigned long long wait_ns, int stall_chunk)
+                                        uint32_t *__restrict__ dev_error, int stall_chunk)
 {
     extern __shared__ __align__(16) int32_t sm[];
     constexpr int nthr = kRowThreads;
-    int32_t *tot = sm;                           // [E]
-    int32_t *pre = tot + align4(E);              // [E]
+    const int nc = ceil_div(chunks, kCountCluster), cl = c / kCountCluster;
+    const int ep = align4(E);                    // workspace rows start 16-byte aligned
+    int32_t *tot = sm;                           // [nc][ep]: the clusters' totals; row 0 the sums
+    int32_t *pre = tot + nc * ep;                // [ep]
     int32_t *base = pre + align4(E);             // [E + 1]
     int32_t *cnt = base + align4(E + 1);         // [kRankWarps][E], 16-byte aligned
     int32_t *ids_s = cnt + E * kRankWarps;       // [tpc * K], 16-byte aligned
     __shared__ int32_t warp_sums[32];
     __shared__ uint32_t s_err;
-    __shared__ int s_ok;
 
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     const int t0 = min(T, c * tpc), t1 = min(T, t0 + tpc);
     const int first = t0 * K, m = (t1 - t0) * K;
-    const int ne_max = ceil_div(E, chunks);
-    const int e0 = min(E, c * ne_max), ne = min(E, e0 + ne_max) - e0;
-    // lane holds 2^lp consecutive chunks of a column (chunks <= 32 << lp)
-    const int lp = chunks <= 32 ? 0 : (chunks <= 64 ? 1 : 2);
-    const int q0 = lane << lp;
     for (int i = tid; i < E * kRankWarps / 4; i += nthr)
         reinterpret_cast<int4 *>(cnt)[i] = make_int4(0, 0, 0, 0);
-    if (tid == 0) {
-        s_err = 0;
-        s_ok = 1;
-    }
+    if (tid == 0) s_err = 0;
     // The chunk's ids are an input of the call, complete before this grid
     // started: the counting kernel's blocks let it start only after their own
     // wait for the kernel before the call.  So they are staged and ranked,
@@ -232,79 +232,33 @@ __device__ __forceinline__ void rank_chunk(const int32_t *__restrict__ ids, int 
     pdl_wait();
     pdl_trigger();
 
-    // 1. this warp's histogram words (word k: column w + (k >> lp) *
-    //    kRankWarps, chunk q0 + k % 2^lp), then each column's prefix over
-    //    the chunks
-    int32_t hv[kColWords];
-#pragma unroll
-    for (int k = 0; k < kColWords; ++k) {
-        const int j = w + (k >> lp) * kRankWarps, q = q0 + (k & ((1 << lp) - 1));
-        hv[k] = j < ne && q < chunks ? ld_l2(ws_cnt + (size_t)q * E + e0 + j) : 0;
-    }
+    // 1. every cluster's totals and this chunk's prefix within its cluster
+    //    (a cluster's first chunk has none) in one round of copies; then
+    //    each expert's total, and its entries in the chunks before this one
+    const bool own_pre = c % kCountCluster != 0;
+    stage_i32(tot, ws_ctot, nc * ep);
+    if (own_pre) stage_i32(pre, ws_pre + (size_t)c * ep, ep);
     if (c == 0) {
         uint32_t err = 0;
         for (int q = tid; q < chunks; q += nthr) err |= ld_relaxed(ws_err + q) & ~kAbandonedBit;
         if (err) atomicOr(&s_err, err);
     }
-#pragma unroll
-    for (int i = 0; i < kColWords; ++i) {
-        const int j = w + i * kRankWarps;
-        if ((i << lp) >= kColWords || j >= ne) break;
-        int sum = 0;
-#pragma unroll
-        for (int k = 0; k < kColWords; ++k)
-            if ((k >> lp) == i) sum += hv[k];
-        int x = sum;
-#pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-            const int y = __shfl_up_sync(kFullMask, x, d);
-            if (lane >= d) x += y;
-        }
-        int run = x - sum;
-#pragma unroll
-        for (int k = 0; k < kColWords; ++k) {
-            const int q = q0 + (k & ((1 << lp) - 1));
-            if ((k >> lp) == i && q < chunks) {
-                ws_cnt[(size_t)q * E + e0 + j] = run;
-                run += hv[k];
-            }
-        }
-        if (lane == 31) ws_tot[e0 + j] = x;
-    }
-
-    // 2. arrive, and wait for the other ranking blocks
-    __threadfence();
+    cp_async_wait_all();
     __syncthreads();
-    if (c == -2 - stall_chunk) return;      // test hook: this block never arrives
-    if (tid == 0) {
-        atomicAdd(ws_sync, 1u);
-        const unsigned long long deadline = global_ns() + wait_ns;
-        while (ld_relaxed(ws_sync) < (uint32_t)chunks) {
-            __nanosleep(32);
-            if (global_ns() > deadline) {
-                s_ok = 0;
-                break;
-            }
-        }
-        __threadfence();
-    }
-    __syncthreads();
-    if (!s_ok) {
-        // the chunk is never ranked: its packing blocks stop waiting
-        if (tid == 0) {
-            atomicOr(ws_err + c, kAbandonedBit);
-            if (dev_error) atomicOr(dev_error, MOE_DEV_ERR_TIMEOUT);
-        }
-        return;
-    }
-
-    // 3. expert offsets, then every entry's slot
-    // (chunk 0's prefixes are all zero)
     for (int e = tid; e < E; e += nthr) {
-        tot[e] = ld_l2(ws_tot + e);
-        if (c) pre[e] = ld_l2(ws_cnt + (size_t)c * E + e);
+        int t = 0, b = own_pre ? pre[e] : 0;
+        for (int k = 0; k < nc; ++k) {
+            const int v = tot[k * ep + e];
+            t += v;
+            if (k < cl) b += v;
+        }
+        tot[e] = t;
+        pre[e] = b;
     }
     __syncthreads();
+
+    // 2. expert offsets, then every entry's slot (chunk 0 has no earlier
+    //    entries)
     block_scan(tot, base, E, warp_sums);
     if (c == 0) {
         for (int e = tid; e < E; e += nthr) {
@@ -338,9 +292,7 @@ __device__ __forceinline__ void rank_chunk(const int32_t *__restrict__ ids, int 
 // At 40 registers both forms keep 6 blocks of 256 threads (48 warps) per SM.
 // The packing blocks stay within them without spilling because the FP8 form
 // quantises after its slots are known (quantising before the wait kept the
-// block's position and slots live across the division calls and spilled);
-// the ranking blocks spill a little, which costs them less than fewer
-// resident packing blocks would.
+// block's position and slots live across the division calls and spilled).
 #ifndef MOE_RANK_DISPATCH_MIN_BLOCKS
 #define MOE_RANK_DISPATCH_MIN_BLOCKS 6
 #endif
@@ -352,8 +304,8 @@ template <int KT, bool kFp8>
 __global__ void __launch_bounds__(kRowThreads, MOE_RANK_DISPATCH_MIN_BLOCKS)
 rank_dispatch_kernel(const int32_t *__restrict__ ids, const uint4 *__restrict__ tokens, int T,
                      int H, int K, int E, int R, int tpc, int chunks,
-                     int32_t *__restrict__ ws_cnt, uint32_t *__restrict__ ws_err,
-                     int32_t *__restrict__ ws_tot, uint32_t *__restrict__ ws_sync,
+                     const int32_t *__restrict__ ws_pre, uint32_t *__restrict__ ws_err,
+                     const int32_t *__restrict__ ws_ctot,
                      int32_t *__restrict__ counts, int32_t *__restrict__ offsets,
                      int32_t *__restrict__ rank_offsets, int32_t *__restrict__ src_token,
                      int32_t *__restrict__ dst_row, uint32_t *__restrict__ dev_error,
@@ -363,9 +315,8 @@ rank_dispatch_kernel(const int32_t *__restrict__ ids, const uint4 *__restrict__ 
     const int k_count = KT > 0 ? KT : K;
     const int b = blockIdx.x;
     if (b < chunks) {
-        rank_chunk(ids, T, k_count, E, R, tpc, chunks, b, ws_cnt, ws_err, ws_tot, ws_sync,
-                   counts, offsets, rank_offsets, src_token, dst_row, dev_error, wait_ns,
-                   stall_chunk);
+        rank_chunk(ids, T, k_count, E, R, tpc, chunks, b, ws_pre, ws_err, ws_ctot, counts,
+                   offsets, rank_offsets, src_token, dst_row, dev_error, stall_chunk);
         return;
     }
     // packing block q covers kRowThreads consecutive pieces of the flat
@@ -438,33 +389,57 @@ rank_dispatch_kernel(const int32_t *__restrict__ ids, const uint4 *__restrict__ 
 }
 
 // The ranking blocks' plan: the layout's chunks, made larger where there
-// would be more than kMaxRankBlocks (fewer chunks also need less workspace
-// than the layout's plan), their shared memory, and whether the ranking
-// blocks' column step fits (each lane holds at most kColWords words).
+// would be more than max_chunks (fewer chunks also need less workspace than
+// the layout's plan), and larger again, a cluster at a time, until the
+// ranking blocks' shared memory fits smem_limit (the clusters' totals
+// shrink with fewer chunks while each chunk's ids grow).
 struct RankPlan {
     bool ok;
     LayoutPlan lp;
     size_t smem;
 };
 
-RankPlan plan_rank(int T, int K, int E)
+RankPlan plan_rank(int T, int K, int E, int max_chunks, size_t smem_limit)
 {
     RankPlan rp{};
     rp.lp = plan_layout(T, K, E);
     if (T <= 0 || rp.lp.single_launch) return rp;
-    // the ranking blocks wait for one another, so all of them must be
-    // resident at once
-    if (rp.lp.chunks > kMaxRankBlocks) {
-        rp.lp.tokens_per_chunk = ceil_div(T, kMaxRankBlocks);
-        rp.lp.chunks = ceil_div(T, rp.lp.tokens_per_chunk);
+    int tpc = rp.lp.tokens_per_chunk, chunks = rp.lp.chunks;
+    if (chunks > max_chunks) {
+        tpc = ceil_div(T, max_chunks);
+        chunks = ceil_div(T, tpc);
     }
-    const int chunks = rp.lp.chunks;
-    const int ne_max = ceil_div(E, chunks);
-    rp.smem = sizeof(int32_t) * ((size_t)2 * align4(E) + align4(E + 1) + (size_t)kRankWarps * E +
-                                 (size_t)rp.lp.tokens_per_chunk * K);
-    rp.ok = chunks <= 32 * kColWords &&
-            ne_max <= (kColWords >> (chunks <= 32 ? 0 : (chunks <= 64 ? 1 : 2))) * kRankWarps;
-    return rp;
+    while (true) {
+        const size_t smem = sizeof(int32_t) * rank_smem_words(chunks, tpc, K, E);
+        if (smem <= smem_limit) {
+            rp.ok = true;
+            rp.lp.tokens_per_chunk = tpc;
+            rp.lp.chunks = chunks;
+            rp.smem = smem;
+            return rp;
+        }
+        if (chunks <= kCountCluster) return rp;
+        tpc = ceil_div(T, chunks - kCountCluster);
+        chunks = ceil_div(T, tpc);
+    }
+}
+
+// Where the ranking blocks' form keeps its state in the workspace, in int32
+// elements from its start, rows of align4(E) elements (16-byte aligned):
+// ws_pre[chunks][E] (each chunk's prefix within its cluster),
+// ws_ctot[clusters][E] (each cluster's totals), then ws_err[chunks].
+struct RankedWorkspaceLayout {
+    size_t ctot, err;
+    size_t bytes;
+};
+
+RankedWorkspaceLayout ranked_workspace_layout(int chunks, int E)
+{
+    RankedWorkspaceLayout w;
+    w.ctot = (size_t)chunks * align4(E);
+    w.err = w.ctot + (size_t)ceil_div(chunks, kCountCluster) * align4(E);
+    w.bytes = sizeof(int32_t) * (w.err + (size_t)chunks);
+    return w;
 }
 
 struct PrefillPlan {
@@ -477,7 +452,7 @@ struct PrefillPlan {
 PrefillPlan plan_prefill(int T, int H, int K, int E, bool fp8)
 {
     PrefillPlan pp{};
-    const RankPlan rp = plan_rank(T, K, E);
+    const RankPlan rp = plan_rank(T, K, E, kMaxRankBlocks, kMaxRankSmem);
     pp.lp = rp.lp;
     pp.smem = rp.smem;
     if (!rp.ok) return pp;
@@ -495,11 +470,17 @@ PrefillPlan plan_prefill(int T, int H, int K, int E, bool fp8)
 }
 
 struct PrefillWorkspace {
-    int32_t *cnt;
+    int32_t *pre;
     uint32_t *err;
-    int32_t *tot;
-    uint32_t *sync;
+    int32_t *ctot;
 };
+
+PrefillWorkspace prefill_workspace(void *workspace, int chunks, int E)
+{
+    const RankedWorkspaceLayout wl = ranked_workspace_layout(chunks, E);
+    int32_t *base = static_cast<int32_t *>(workspace);
+    return {base, reinterpret_cast<uint32_t *>(base + wl.err), base + wl.ctot};
+}
 
 template <int KT, bool kFp8>
 cudaError_t run_prefill(const PrefillPlan &pp, const int32_t *ids, const void *tokens, int T,
@@ -515,8 +496,9 @@ cudaError_t run_prefill(const PrefillPlan &pp, const int32_t *ids, const void *t
     const unsigned grid = (unsigned)(pp.lp.chunks + pp.pack_blocks);   // no packing blocks: layout only
     return launch_pdl(fn, dim3(grid), dim3(kRowThreads), pp.smem, s, ids,
                       static_cast<const uint4 *>(tokens), T, H, K, E, R,
-                      pp.lp.tokens_per_chunk, pp.lp.chunks, ws.cnt, ws.err, ws.tot, ws.sync,
-                      counts, offsets, rank_offsets, src_token, dst_row, dev_error,
+                      pp.lp.tokens_per_chunk, pp.lp.chunks, (const int32_t *)ws.pre, ws.err,
+                      (const int32_t *)ws.ctot, counts, offsets, rank_offsets, src_token,
+                      dst_row, dev_error,
                       static_cast<uint8_t *>(packed), scales, wait_ns, stall_chunk);
 }
 
@@ -552,8 +534,22 @@ bool layout_dispatch_prefill(int T, int H, int K, int E, int fp8)
 
 bool layout_ranked(int T, int K, int E)
 {
-    const RankPlan rp = plan_rank(T, K, E);
-    return rp.ok && rp.smem <= kMaxRankOnlySmem;
+    return plan_rank(T, K, E, kMaxRankOnlyBlocks, kMaxRankOnlySmem).ok;
+}
+
+size_t ranked_workspace_bytes(int T, int K, int E)
+{
+    // both forms' chunks: moe_layout's ranking-only grid and
+    // moe_layout_dispatch's rank-and-pack grid
+    size_t bytes = 0;
+    for (const RankPlan &rp : {plan_rank(T, K, E, kMaxRankOnlyBlocks, kMaxRankOnlySmem),
+                               plan_rank(T, K, E, kMaxRankBlocks, kMaxRankSmem)}) {
+        if (rp.ok) {
+            const size_t b = ranked_workspace_layout(rp.lp.chunks, E).bytes;
+            if (b > bytes) bytes = b;
+        }
+    }
+    return bytes;
 }
 
 cudaError_t launch_layout_ranked(const int32_t *topk_ids, int T, int K, int E, int R,
@@ -561,20 +557,17 @@ cudaError_t launch_layout_ranked(const int32_t *topk_ids, int T, int K, int E, i
                                  int32_t *rank_offsets, int32_t *src_token, int32_t *dst_row,
                                  uint32_t *dev_error, void *workspace, cudaStream_t stream)
 {
-    const RankPlan rp = plan_rank(T, K, E);
-    if (!rp.ok || rp.smem > kMaxRankOnlySmem) return cudaErrorInvalidValue;
+    const RankPlan rp = plan_rank(T, K, E, kMaxRankOnlyBlocks, kMaxRankOnlySmem);
+    if (!rp.ok) return cudaErrorInvalidValue;
     PrefillPlan pp{};
     pp.use = true;
     pp.lp = rp.lp;
     pp.smem = rp.smem;
     pp.pack_blocks = 0;                 // the grid is the ranking blocks alone
-    const WorkspaceLayout wl = workspace_layout(pp.lp.chunks, E);
-    int32_t *base = static_cast<int32_t *>(workspace);
-    const PrefillWorkspace ws{base, reinterpret_cast<uint32_t *>(base + wl.err), base + wl.tot,
-                              reinterpret_cast<uint32_t *>(base + wl.sync)};
+    const PrefillWorkspace ws = prefill_workspace(workspace, pp.lp.chunks, E);
     // no packing blocks poll dst_row, so it needs no pending marks
-    cudaError_t e = launch_layout_count(topk_ids, T, K, E, pp.lp, ws.cnt, ws.err, dev_error,
-                                        nullptr, ws.sync, stream);
+    cudaError_t e = launch_layout_count(topk_ids, T, K, E, pp.lp, ws.pre, ws.err, dev_error,
+                                        nullptr, stream, 256, ws.ctot);
     if (e != cudaSuccess) return e;
     return run_prefill_k<false>(pp, topk_ids, nullptr, T, 8, K, E, R, ws, expert_counts,
                                 expert_offsets, rank_offsets, src_token, dst_row, dev_error,
@@ -592,12 +585,9 @@ cudaError_t launch_layout_dispatch_prefill(const int32_t *topk_ids, const void *
 {
     const PrefillPlan pp = plan_prefill(T, H, K, E, fp8 != 0);
     if (!pp.use) return cudaErrorInvalidValue;
-    const WorkspaceLayout wl = workspace_layout(pp.lp.chunks, E);
-    int32_t *base = static_cast<int32_t *>(workspace);
-    const PrefillWorkspace ws{base, reinterpret_cast<uint32_t *>(base + wl.err), base + wl.tot,
-                              reinterpret_cast<uint32_t *>(base + wl.sync)};
-    cudaError_t e = launch_layout_count(topk_ids, T, K, E, pp.lp, ws.cnt, ws.err, dev_error,
-                                        dst_row, ws.sync, stream, 512);
+    const PrefillWorkspace ws = prefill_workspace(workspace, pp.lp.chunks, E);
+    cudaError_t e = launch_layout_count(topk_ids, T, K, E, pp.lp, ws.pre, ws.err, dev_error,
+                                        dst_row, stream, 512, ws.ctot);
     if (e != cudaSuccess) return e;
     if (wait_ns == 0) wait_ns = kWaitNs;
     if (fp8)
@@ -612,16 +602,12 @@ cudaError_t launch_layout_dispatch_prefill(const int32_t *topk_ids, const void *
 }  // namespace moe
 
 // Test hook, deliberately absent from the public header: the large-batch
-// path of moe_layout_dispatch with a chosen bound on every wait (for a
-// ranked chunk, and the ranking blocks' wait for one another) and
+// path of moe_layout_dispatch with a chosen bound on every wait for a
+// ranked chunk and
 //  * stall_chunk >= 0: that chunk never ranked (its ranking block stops
-//    after the arrival barrier, before writing the slots, which stay
-//    pending).  The chunk's packing blocks' waits expire: they set
-//    MOE_DEV_ERR_TIMEOUT and skip its rows; every other row is packed;
-//  * stall_chunk <= -2: ranking block -2 - stall_chunk never arrives at the
-//    barrier, so every other ranking block's wait expires: no chunk is
-//    ranked, every packing block's wait ends (at once for chunks marked
-//    abandoned), and the error word is MOE_DEV_ERR_TIMEOUT;
+//    before writing the slots, which stay pending).  The chunk's packing
+//    blocks' waits expire: they set MOE_DEV_ERR_TIMEOUT and skip its rows;
+//    every other row is packed;
 //  * stall_chunk == -1: the normal call.
 // Tests use it to see the bounded waits expire with the context still
 // usable.  Arguments are checked by the caller (tests only).

@@ -80,10 +80,11 @@ MOE_API const char *moe_status_string(moe_status_t status);
 MOE_API size_t moe_layout_workspace_bytes(int32_t T, int32_t K, int32_t E);
 
 /* Number of kernel launches moe_layout makes for these sizes: 1 when the
- * whole layout fits one launch of self-counting blocks, 2 (count, then
- * ranking blocks that exchange the chunk histograms among themselves) when
- * that plan fits, otherwise 3 (count, scan, rank; e.g. E near 1024).  0 for
- * invalid sizes.  A query: nothing is launched. */
+ * whole layout fits one launch of self-counting blocks, 2 (count in
+ * clusters of blocks that sum their histograms together, then one ranking
+ * block per chunk) when the ranking blocks' shared memory fits, otherwise 3
+ * (count, scan, rank; large batches with E near 1024).  0 for invalid
+ * sizes.  A query: nothing is launched. */
 MOE_API int32_t moe_layout_kernels(int32_t T, int32_t K, int32_t E);
 
 /*
@@ -299,8 +300,7 @@ MOE_API moe_status_t moe_dispatch_recv(const void *priv, const float *priv_scale
  * moe_layout_workspace_bytes(T,K,E) bytes always suffices; the single-kernel
  * path uses none).  dev_error gets moe_layout's bits and, on the two-launch
  * path, MOE_DEV_ERR_TIMEOUT when a bounded wait (1 s) expired: a packing
- * block's wait for its chunk's slots, or a ranking block's wait for the
- * other ranking blocks; the outputs are then unspecified.
+ * block's wait for its chunk's slots; the outputs are then unspecified.
  */
 MOE_API moe_status_t moe_layout_dispatch(const int32_t *topk_ids, const void *tokens,
                                          int32_t T, int32_t H, int32_t K, int32_t E,

@@ -100,20 +100,23 @@ def test_layout_dispatch_plan_query(lib):
     # decode shapes run as one kernel; prefill shapes as the counting kernel
     # plus one rank-and-pack grid; shapes whose ranking blocks would need too
     # much shared memory for the packing blocks' occupancy (E = 1024) as
-    # count, scan, rank, dispatch
+    # moe_layout's launches and then the dispatch kernel
     assert moe.moe_layout_dispatch_kernels(128, 7168, 8, 256, False) == 1
     assert moe.moe_layout_dispatch_kernels(256, 7168, 8, 256, True) == 1
     assert moe.moe_layout_dispatch_kernels(4096, 7168, 8, 384, False) == 2
     assert moe.moe_layout_dispatch_kernels(16384, 4096, 8, 128, True) == 2
+    assert moe.moe_layout_dispatch_kernels(16384, 7168, 8, 256, True) == 2
     assert moe.moe_layout_dispatch_kernels(1000, 4096, 8, 128, False) == 2
     assert moe.moe_layout_dispatch_kernels(5000, 65536, 8, 16, False) == 2
-    assert moe.moe_layout_dispatch_kernels(2000, 1024, 8, 1024, False) == 4
-    # moe_layout alone: one self-counting launch, count + ranking blocks, or
-    # count, scan, rank
+    assert moe.moe_layout_dispatch_kernels(2000, 1024, 8, 1024, False) == 3    # 2 + dispatch
+    assert moe.moe_layout_dispatch_kernels(30000, 1024, 8, 1024, False) == 4   # 3 + dispatch
+    # moe_layout alone: one self-counting launch, count + ranking blocks
+    # (while the ranking blocks' shared memory fits), or count, scan, rank
     assert moe.moe_layout_kernels(128, 8, 256) == 1
     assert moe.moe_layout_kernels(4096, 8, 384) == 2                 # count + ranking
     assert moe.moe_layout_kernels(16384, 8, 128) == 2
-    assert moe.moe_layout_kernels(2000, 8, 1024) == 3                # count, scan, rank
+    assert moe.moe_layout_kernels(2000, 8, 1024) == 2
+    assert moe.moe_layout_kernels(30000, 8, 1024) == 3               # count, scan, rank
     assert moe.moe_layout_kernels(16384, 8, 100000) == 0             # invalid E
     assert moe.moe_layout_dispatch_kernels(512, 7168, 8, 256, False) == 2
     assert moe.moe_layout_dispatch_kernels(0, 128, 4, 16, False) == 1

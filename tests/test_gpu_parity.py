@@ -61,7 +61,7 @@ SHAPES = [  # T, K, E, R: single kernel, count + ranking, count/scan/rank, ragge
     (1500, 5, 40, 5), (4097, 2, 1024, 16), (5000, 8, 1024, 1024),
     (20000, 8, 384, 48), (70001, 4, 96, 12), (3000, 32, 64, 4),
     (300000, 1, 1, 1), (500, 8, 256, 32), (1365, 3, 5, 5), (3000, 3, 16, 4),
-    (4096, 1, 1024, 2), (130000, 8, 128, 16),
+    (4096, 1, 1024, 2), (130000, 8, 128, 16), (30000, 8, 1024, 64),
     # just above one kernel's size, T = 129 at K = 32, Qwen3-sized
     (1025, 4, 16, 4), (129, 32, 64, 8), (16384, 8, 128, 16),
 ]
