@@ -6,6 +6,7 @@ import os
 import subprocess
 import sys
 
+import numpy as np
 import pytest
 
 import combine_moe_layout_05_gb300 as moe
@@ -138,6 +139,26 @@ def test_layout_dispatch_host_checks(lib):
     assert f(*args(packed=FAKE + 4)) == 2
     assert f(*args(fp8=1, scales=FAKE + 2)) == 2
     assert f(*args(T=4096, H=7168, K=8, E=384, R=48)) == 4       # needs workspace
+
+
+def test_workspace_fits_the_static_scratch(lib):
+    # moe_layout_static's documented bound: every batch moe_layout accepts
+    # with E >= 2 needs at most MOE_LAYOUT_STATIC_SCRATCH_BYTES of workspace
+    # (both multi-launch forms: count/scan/rank and counting clusters plus
+    # ranking blocks); with E = 1 only batches of more than 12.5 M entries
+    # need more
+    scratch = 96 << 10
+    Ts = sorted({int(x) for x in np.geomspace(500, 20_000_000, 60)} | {4097, 16384, 30000})
+    for E in (1, 2, 3, 8, 64, 128, 256, 384, 512, 1000, 1024):
+        for K in (1, 2, 8, 32):
+            if K > E:
+                continue
+            for T in Ts:
+                if moe.moe_layout_kernels(T, K, E) == 0:
+                    continue                          # not accepted
+                ws = moe.moe_layout_workspace_bytes(T, K, E)
+                if E >= 2 or T * K <= 12_500_000:
+                    assert ws <= scratch, (T, K, E, ws)
 
 
 def test_layout_size_limit(lib):

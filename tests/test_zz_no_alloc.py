@@ -72,7 +72,7 @@ def _with_workspace(ids, E, R):
 def test_static_scratch_matches_workspace_layout_twice(lib):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
-    # large batches: count -> scan -> rank on the scratch array, one call
+    # large batches: the multi-launch layout on the scratch array, one call
     # after another, each reusing what the previous one left there
     rng = np.random.default_rng(5)
     big = [(32768, 8, 128, 16), (20000, 8, 384, 48)]
