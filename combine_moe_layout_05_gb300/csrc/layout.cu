@@ -127,22 +127,35 @@ layout_count_kernel(const int32_t *__restrict__ ids, int T, int K, int E, int tp
         const int32_t *peer = cluster.map_shared_rank(hist, j);
         const int q = g * kCountCluster + j;
         const size_t ep = (size_t)align4(E);     // row stride: rows start 16-byte aligned
-        for (int b = 0; b < n; b += nthr) {  // whole warps take the shuffles
-            const int i = b + tid;
+        // every read of the other blocks' histograms first (n <= 1024 <=
+        // kPeerReads * nthr), then this block announces that it is done
+        // with them, and waits for the others only before it leaves
+        constexpr int kPeerReads = 4;
+        int v[kPeerReads];
+#pragma unroll
+        for (int it = 0; it < kPeerReads; ++it) {
+            const int i = it * nthr + tid;
+            v[it] = i < n ? peer[e_lo + i / kCountCluster] : 0;
+        }
+        asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+#pragma unroll
+        for (int it = 0; it < kPeerReads; ++it) {
+            if (it * nthr >= n) break;           // whole warps take the shuffles
+            const int i = it * nthr + tid;
             const int e = e_lo + i / kCountCluster;
-            const int v = i < n ? peer[e] : 0;
-            int x = v;
+            int x = v[it];
 #pragma unroll
             for (int d = 1; d < kCountCluster; d <<= 1) {
                 const int y = __shfl_up_sync(kFullMask, x, d, kCountCluster);
                 if (j >= d) x += y;
             }
             if (i < n) {
-                if (q < chunks) ws_cnt[q * ep + e] = x - v;
+                if (q < chunks) ws_cnt[q * ep + e] = x - v[it];
                 if (j == kCountCluster - 1) ws_ctot[g * ep + e] = x;
             }
         }
-        cluster.sync();                      // no block leaves while its histogram is read
+        // no block leaves while another may still read its histogram
+        asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
     }
 }
 
